@@ -1,0 +1,337 @@
+"""Benchmark of the MoE decode layer on one GB300 (replicas on N GPUs).
+
+One step = one decode-layer call of the DeepSeek-V3-shaped layer (H=7168, 256
+routed experts, top-8, I = I_s = 2048, FP8 E4M3 weights with fp32 128x128
+block scales) at each of M = 1, 8 and 32 tokens, on distinct seeded inputs.
+The weights (11.3 GB) are random-init and resident in HBM; L2 is flushed
+(a 512 MB write) before every layer call, outside the timed events.
+
+Prints one JSON line: tokens/s over all layer calls (device time, CUDA
+events), the per-M microseconds per layer and HBM GB/s, the roofline of the
+expert kernel (algorithmic bytes / its measured duration vs the measured HBM
+copy bandwidth), the end-to-end figure through the public API with host
+buffers, the CPU oracle as a reported baseline, clocks and launch counts.
+
+--impl reference times the CPU oracle alone, on the same workload (a bounded
+sample per step), and prints the same kind of line with "impl": "reference".
+"""
+
+from __future__ import annotations
+
+import os
+
+# the oracle baseline is single-threaded: pin BLAS before numpy loads
+for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse
+import json
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_decode_layer_bf16_gb300 import synth  # noqa: E402
+from moe_decode_layer_bf16_gb300.dims import DSV3  # noqa: E402
+
+MS = (1, 8, 32)
+METRIC = "MoE decode layer tokens/s (DeepSeek-V3-shaped layer, M=1,8,32)"
+UNIT = "tokens/s"
+WORKLOAD = "deepseek-v3-shaped MoE decode layer, H=7168 E=256 k=8 I=Is=2048, M in {1,8,32}"
+# bytes of one expert: fp8 w13 [2I,H] + w2 [H,I] + fp32 128x128 scales
+EXPERT_BYTES = 2 * DSV3.inter * DSV3.hidden + DSV3.hidden * DSV3.inter + 4 * (
+    (2 * DSV3.inter // 128) * (DSV3.hidden // 128) + (DSV3.hidden // 128) * (DSV3.inter // 128))
+ROUTER_BYTES = DSV3.num_experts * DSV3.hidden * 2
+
+
+def layer_bytes(M: int, unique: int) -> int:
+    """Algorithmic HBM bytes of one layer call: the activated experts' and the
+    shared expert's weights, the router weight, x/residual in, out/residual_out
+    out (bf16), and the norm gain."""
+    return (unique + 1) * EXPERT_BYTES + ROUTER_BYTES + 4 * M * DSV3.hidden * 2 + DSV3.hidden * 2
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi samples of the SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap,utilization.gpu")
+
+    def __init__(self, index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 7:
+                continue
+            try:
+                util = float(f[6])
+                if util > 0:
+                    sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[2:6]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not mx:
+            return None
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(mx)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(seed: int = 0):
+    """One M=1 layer of the same shape, on the CPU oracle: the routing picks
+    the experts, only those are drawn.  Returns (seconds, description)."""
+    from oracle import moe_oracle as orc
+
+    dims = DSV3
+    x, res = synth.make_tokens(1, dims.hidden, seed=seed)
+    lw = synth.make_layer(dims, seed=seed, experts=[])  # router, shared expert, gain
+
+    def np_(t):
+        return None if t is None else (t.float().numpy().astype(np.float64) if t.dtype == torch.bfloat16
+                                       else t.numpy())
+
+    x64 = x.float().numpy().astype(np.float64)
+    _, _, _, ids, _ = orc.route(x64, np_(lw["router_w"]), None, dims.top_k, dims.routed_scaling)
+    w13, w13_s, w2, w2_s = {}, {}, {}, {}
+    for e in sorted(set(ids.reshape(-1).tolist())):
+        a, b, c, d = synth.make_expert(dims, e, seed=seed)
+        w13[e], w13_s[e], w2[e], w2_s[e] = a.numpy(), b.numpy(), c.numpy(), d.numpy()
+    L = orc.Layer(router_w=np_(lw["router_w"]), sel_bias=None, w13=w13, w13_s=w13_s, w2=w2, w2_s=w2_s,
+                  sw13=np_(lw["sw13"]), sw13_s=np_(lw["sw13_s"]), sw2=np_(lw["sw2"]), sw2_s=np_(lw["sw2_s"]),
+                  gain=np_(lw["gain"]), top_k=dims.top_k, routed_scaling=dims.routed_scaling,
+                  swiglu_limit=dims.swiglu_limit, rms_eps=dims.rms_eps, e8m0=dims.e8m0)
+    t0 = time.perf_counter()
+    orc.moe_decode_layer(L, x64, np_(res))
+    dt = time.perf_counter() - t0
+    return dt, "one M=1 layer call (router, 8 routed + shared expert dequantised and applied, boundary)"
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    for _ in range(args.warmup):
+        oracle_sample(seed=0)
+    times = []
+    for s in range(args.steps):
+        dt, desc = oracle_sample(seed=s)
+        times.append(dt)
+    total = sum(times)
+    value = args.steps / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "sample": "M=1 per step"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+
+def run_ours(args, world, rank, local):
+    import moe_decode_layer_bf16_gb300 as m
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dims = DSV3
+    lw = synth.make_layer(dims, seed=0, device=dev)
+    layer = m.MoeDecodeLayer(dims, lw, max_tokens=max(MS), device=dev)
+    inputs = {M: synth.make_tokens(M, dims.hidden, seed=100 + M, device=dev) for M in MS}
+    outs = {M: (torch.empty_like(inputs[M][0]), torch.empty_like(inputs[M][1])) for M in MS}
+    ids = {M: torch.empty((M, dims.top_k), dtype=torch.int32, device=dev) for M in MS}
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call(M, events=None):
+        x, res = inputs[M]
+        out, ro = outs[M]
+        if events is None:
+            m.moe_decode_layer(dims, lw, x, res, out, ro, layer.workspace, topk_ids=ids[M])
+        else:
+            m.moe_decode_layer_traced(dims, lw, x, res, out, ro, layer.workspace, events, topk_ids=ids[M])
+
+    # warm-up
+    for _ in range(args.warmup):
+        for M in MS:
+            flush.zero_()
+            call(M)
+    torch.cuda.synchronize()
+    st = layer.status()
+    if st != m.MOE_OK:
+        raise RuntimeError(f"device status {st}")
+    unique = {M: int(torch.unique(ids[M]).numel()) for M in MS}
+
+    # timed region: per layer call, events around its three kernels
+    ev = {(s, M): [torch.cuda.Event(enable_timing=True) for _ in range(4)] for s in range(args.steps) for M in MS}
+    clocks = Clocks(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for s in range(args.steps):
+        for M in MS:
+            flush.zero_()
+            call(M, ev[(s, M)])
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    barrier(world)
+    clk = clocks.stop()
+
+    per_m = {}
+    total_ms = 0.0
+    exp_ms_all, exp_bytes_all = 0.0, 0
+    for M in MS:
+        layer_ms = [ev[(s, M)][0].elapsed_time(ev[(s, M)][3]) for s in range(args.steps)]
+        exp_ms = [ev[(s, M)][1].elapsed_time(ev[(s, M)][2]) for s in range(args.steps)]
+        rt_ms = [ev[(s, M)][0].elapsed_time(ev[(s, M)][1]) for s in range(args.steps)]
+        nm_ms = [ev[(s, M)][2].elapsed_time(ev[(s, M)][3]) for s in range(args.steps)]
+        total_ms += sum(layer_ms)
+        exp_ms_all += sum(exp_ms)
+        eb = (unique[M] + 1) * EXPERT_BYTES
+        exp_bytes_all += eb * args.steps
+        lb = layer_bytes(M, unique[M])
+        us = 1e3 * statistics.median(layer_ms)
+        per_m[str(M)] = {"us_per_layer": round(us, 2), "tokens_per_s": round(M * 1e6 / us, 1),
+                         "unique_experts": unique[M], "layer_bytes": lb,
+                         "layer_gbps": round(lb / us / 1e3, 1),
+                         "us_router": round(1e3 * statistics.median(rt_ms), 2),
+                         "us_experts": round(1e3 * statistics.median(exp_ms), 2),
+                         "us_boundary": round(1e3 * statistics.median(nm_ms), 2)}
+    # replicas: every rank runs the same steps; the job's time is the slowest rank's
+    total_ms = max_over_ranks(total_ms, world)
+    value = sum(MS) * args.steps * world / (total_ms / 1e3)
+
+    peak, peak_kind = load_peaks()
+    achieved = exp_bytes_all / (exp_ms_all / 1e3) / 1e9
+    for M in MS:
+        per_m[str(M)]["frac_of_8TBs"] = round(per_m[str(M)]["layer_gbps"] / 8000.0, 3)
+        per_m[str(M)]["frac_of_measured"] = round(per_m[str(M)]["layer_gbps"] / peak, 3)
+
+    # end to end through the public API with host buffers
+    h_in = {M: [t.cpu().pin_memory() for t in inputs[M]] for M in MS}
+    h_out = {M: [torch.empty_like(t, device="cpu").pin_memory() for t in inputs[M]] for M in MS}
+    d_in = {M: [torch.empty_like(t) for t in inputs[M]] for M in MS}
+    e2e_ms = 0.0
+    for rep in range(-1, args.steps):
+        for M in MS:
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for d, h in zip(d_in[M], h_in[M]):
+                d.copy_(h, non_blocking=True)
+            out, ro = layer(d_in[M][0], d_in[M][1], out=outs[M][0], residual_out=outs[M][1])
+            h_out[M][0].copy_(out, non_blocking=True)
+            h_out[M][1].copy_(ro, non_blocking=True)
+            e1.record()
+            e1.synchronize()
+            if rep >= 0:
+                e2e_ms += e0.elapsed_time(e1)
+    e2e_value = sum(MS) * args.steps / (e2e_ms / 1e3)
+    io_bytes = sum(2 * M * dims.hidden * 2 for M in MS)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, desc = oracle_sample(seed=0)
+        cpu = {"value": 1.0 / dt, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8",
+        "data": "synthetic (seeded random-init weights and tokens)",
+        "config": {"workload": WORKLOAD, "tokens_per_step": sum(MS), "l2": "flushed (512 MB write) before every layer call",
+                   "weights": "fp8-e4m3 with fp32 128x128 block scales; router bf16; activations bf16 in/out",
+                   "parallelism": "replicas" if world > 1 else "single GPU", "per_m": per_m,
+                   "wall_s_timed": round(wall, 4)},
+        "roofline": {"bound": "hbm", "kernel": "experts_kernel", "achieved": round(achieved, 1),
+                     "peak": peak, "peak_kind": f"{peak_kind} HBM copy bandwidth", "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes},
+        "gpu_launches": m.LAUNCHES_PER_LAYER * len(MS) * args.steps,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,205 @@
+/*
+ * moe_decode.h -- C ABI of the GB300 (sm_103a) MoE decode-layer library
+ * (libmoe_decode.so).
+ *
+ * One low-batch decode step of a DeepSeek/GLM-style MoE layer, as the vLLM
+ * specialized-decode executor pages describe it:
+ *   [decode page] vllm.models.glm5next.nvidia.specialized_decode.runtime.decode
+ *   [draft page]  vllm.models.glm5next.nvidia.specialized_decode.runtime.draft
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are DEVICE pointers to dense row-major arrays that
+ *     the caller allocated on the current CUDA device.  The library never
+ *     allocates, frees or synchronises (moe_device_status excepted), and keeps
+ *     no pointer past return.  Weights are read, never written ("reads the
+ *     backbone, never modifies it", [decode page] class SpecializedDecode).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is only enqueued; every call is stream-ordered.
+ *   - Return value: MOE_OK or an error code below.  Argument errors are found
+ *     on the host before anything is enqueued.  There is no CPU fallback:
+ *     an unsupported shape returns MOE_ERR_UNSUPPORTED and the caller decides
+ *     (the pages' executors likewise refuse unsupported configurations and
+ *     leave the step to the stock forward).
+ *   - bf16 = IEEE bfloat16 stored as uint16; fp8 = E4M3 (OCP "E4M3FN") codes
+ *     stored as uint8; fp32 = IEEE float.
+ */
+#ifndef MOE_DECODE_H
+#define MOE_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,          /* null pointer, negative size, bad value  */
+  MOE_ERR_UNSUPPORTED = 2,          /* shape outside the supported range        */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes below the *_workspace_size     */
+  MOE_ERR_CUDA = 4,                 /* a CUDA runtime call or launch failed     */
+  MOE_ERR_DEVICE_TIMEOUT = 5        /* a bounded device-side wait gave up       */
+};
+
+/*
+ * Layer dimensions and switches ([decode page] LayerStages._build_mega: the
+ * routed-expert kernel is built from num_experts_per_tok, swiglu_limit,
+ * routed_scaling_factor and the e8m0 switch; only sigmoid scoring with
+ * n_group == 1 and norm_topk_prob is accepted, which is the only routing this
+ * library implements).
+ *   hidden        H, multiple of 128, <= 16384
+ *   inter         I (moe_intermediate_size), multiple of 128, <= 8192
+ *   shared_inter  I_s of the shared expert, multiple of 128 (0 = none)
+ *   num_experts   E routed experts, 1 <= E <= 512
+ *   top_k         k, 1 <= k <= min(E, 16)
+ *   routed_scaling  multiplies the normalised top-k weights
+ *   swiglu_limit  L in h = silu(min(g, L)) * clamp(u, -L, L); +inf disables it
+ *   rms_eps       epsilon inside the RMSNorm square root
+ *   e8m0          nonzero: activation block scales are rounded up to powers of
+ *                 two (the weights' scales are then expected to be powers of
+ *                 two as well; they are used as given either way)
+ */
+typedef struct moe_layer_dims {
+  int hidden;
+  int inter;
+  int shared_inter;
+  int num_experts;
+  int top_k;
+  float routed_scaling;
+  float swiglu_limit;
+  float rms_eps;
+  int e8m0;
+} moe_layer_dims;
+
+/*
+ * Weights of one MoE layer ([decode page] LayerStages._build_mega:
+ * w13_weight, w13_weight_scale_inv, w2_weight, w2_weight_scale_inv, the
+ * shared expert's gate_up_proj / down_proj with their weight_scale_inv, the
+ * gate's bf16 weight and e_score_correction_bias).
+ *   router_w  bf16 [E, H]
+ *   sel_bias  fp32 [E] or NULL: added to the sigmoid scores for selection only
+ *   w13       fp8 [E, 2I, H]: rows [0, I) gate, rows [I, 2I) up
+ *   w13_s     fp32 [E, 2I/128, H/128]: scale of each 128x128 block (w = code * s)
+ *   w2        fp8 [E, H, I];  w2_s fp32 [E, H/128, I/128]
+ *   sw13, sw13_s, sw2, sw2_s: the shared expert alike, without the E dimension
+ *             (NULL when shared_inter == 0)
+ *   norm_gain bf16 [H]: gain of the RMSNorm at the layer boundary
+ * All weight pointers must be 16-byte aligned.
+ */
+typedef struct moe_layer_weights {
+  const void *router_w;
+  const float *sel_bias;
+  const uint8_t *w13;
+  const float *w13_s;
+  const uint8_t *w2;
+  const float *w2_s;
+  const uint8_t *sw13;
+  const float *sw13_s;
+  const uint8_t *sw2;
+  const float *sw2_s;
+  const void *norm_gain;
+} moe_layer_weights;
+
+/* Bytes of device workspace moe_decode_layer needs for up to max_tokens
+ * tokens (1 <= max_tokens, max_tokens * top_k <= 4096). */
+int moe_decode_workspace_size(const moe_layer_dims *dims, int max_tokens, size_t *bytes);
+
+/* Zero a workspace (moe_decode_layer's or splitk_gemm_bf16's) once before its
+ * first use.  Calls leave their counters at zero for the next call, so this
+ * is needed only once per buffer. */
+int moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * One decode step of the MoE layer plus the layer boundary, for M tokens:
+ *   logits = x . router_w^T (fp32); s = sigmoid(logits); sel = s + sel_bias;
+ *   ids = top-k of sel (descending; ties to the lower id);
+ *   w = s[ids] / sum(s[ids]) * routed_scaling;
+ *   route order: stable counting sort of r = t*k + j by expert;
+ *   per routed expert and for the shared expert (weight 1), on FP8 activations
+ *   quantised per token per 128-column group (scale = amax/448):
+ *     [g; u] = x . w13^T, h = silu(min(g, L)) * clamp(u, -L, L),
+ *     h quantised likewise, y = h . w2^T;
+ *   m = sum_j w_j * y_(t,j) + y_shared;  r' = m + residual;
+ *   residual_out = bf16(r');  out = bf16(r' * rsqrt(mean(r'^2) + eps) * gain).
+ * ([decode page] LayerStages._mega_moe / _router; [draft page]
+ * SpecializedDraft.reduced_norm: "norm(x + residual) and the new residual".)
+ *
+ *   x, residual      bf16 [M, H] inputs (may not alias the outputs)
+ *   out, residual_out  bf16 [M, H] outputs
+ *   topk_ids         int32 [M, k] or NULL; topk_w fp32 [M, k] or NULL
+ *   sorted_routes    int32 [M*k] or NULL: expanded route indices grouped by
+ *                    expert (ascending), ascending within an expert
+ *   expert_offsets   int32 [E+1] or NULL: start of each expert's routes
+ *   workspace        from moe_decode_workspace_size(dims, max_tokens >= M),
+ *                    zeroed once by moe_workspace_init; one workspace must not
+ *                    be used by two calls that may run concurrently
+ * M == 0 is a no-op.  Launches exactly three kernels (router + top-k + route
+ * order; the expert kernel; finalize + residual + RMSNorm).
+ */
+int moe_decode_layer(const moe_layer_dims *dims, const moe_layer_weights *w, int M,
+                     const void *x, const void *residual, void *out, void *residual_out,
+                     int32_t *topk_ids, float *topk_w, int32_t *sorted_routes,
+                     int32_t *expert_offsets, void *workspace, size_t ws_bytes,
+                     void *stream);
+
+/* moe_decode_layer that also records four CUDA events (cudaEvent_t passed as
+ * void*) on `stream`: events[0] before the router kernel, [1] before the
+ * expert kernel, [2] before the boundary kernel, [3] after it, so that a
+ * caller can time each kernel.  The events are created by the caller. */
+int moe_decode_layer_traced(const moe_layer_dims *dims, const moe_layer_weights *w, int M,
+                            const void *x, const void *residual, void *out, void *residual_out,
+                            int32_t *topk_ids, float *topk_w, int32_t *sorted_routes,
+                            int32_t *expert_offsets, void *workspace, size_t ws_bytes,
+                            void *stream, void *const *events);
+
+/* Bytes of workspace splitk_gemm_bf16 needs for this shape. */
+int splitk_gemm_workspace_size(int M, int N, int K, size_t *bytes);
+
+/*
+ * Split-K BF16 projection ([draft page] module docstring: the draft's BF16
+ * projections such as eh_proj run a split-K GEMM above two tokens;
+ * SpecializedDraft.run):
+ *   C[M, N] = alpha * A[M, K] . W[N, K]^T, fp32 accumulation.
+ *   A bf16 [M, K]; W bf16 [N, K]; C bf16 [M, N] (c_fp32 == 0) or fp32 [M, N].
+ *   1 <= M <= 256, N % 16 == 0, K % 128 == 0; A, W 16-byte aligned.
+ * The K dimension is divided over the whole GPU (stream-K); partial sums are
+ * reduced in a fixed order, so results are deterministic.
+ */
+int splitk_gemm_bf16(const void *A, const void *W, void *C, int c_fp32, int M, int N, int K,
+                     float alpha, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * Layer boundary: optional weighted top-k finalize, residual add, RMSNorm
+ * ([draft page] SpecializedDraft.reduced_norm; [decode page] _mega_moe hands
+ * the routed rows over unfinalized, in expanded order, for this step):
+ *   m[t] = (x ? x[t] : 0) + (rows ? sum_j route_w[t, j] * rows[t*k + j] : 0)
+ *          + (shared ? shared[t] : 0)
+ *   r' = m + residual;  residual_out = bf16(r');
+ *   out = bf16(bf16(r') * rsqrt(mean(bf16(r')^2) + eps) * gain)
+ *   x bf16 [M, H] or NULL; residual, gain bf16; rows fp32 [M*k, H] or NULL;
+ *   route_w fp32 [M, k] (needed with rows); shared fp32 [M, H] or NULL;
+ *   out, residual_out bf16 [M, H].  H % 128 == 0, H <= 16384.
+ */
+int rmsnorm_residual(const void *x, const void *residual, const void *gain, int M, int H,
+                     float eps, const float *rows, const float *route_w, int k,
+                     const float *shared, void *out, void *residual_out, void *stream);
+
+/* Read and clear the device status word of a moe_decode_layer workspace:
+ * MOE_OK, or MOE_ERR_DEVICE_TIMEOUT when a bounded wait inside the expert
+ * kernel gave up.  Synchronises `stream`; meant for tests and diagnostics. */
+int moe_device_status(void *ws, void *stream);
+
+/* Test hook: nonzero `fault` makes the next moe_decode_layer calls on this
+ * workspace withhold one expert's ready signal, so that the waits on it run
+ * out (about 0.2 s) and report MOE_ERR_DEVICE_TIMEOUT.  Nothing faults. */
+int moe_debug_set_fault(void *ws, int fault, void *stream);
+
+/* Text of a status code. */
+const char *moe_status_str(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_DECODE_H */

@@ -1,0 +1,317 @@
+// C ABI of libmoe_decode.so (declared in include/moe_decode.h): argument
+// checks, workspace layout and kernel launches.  Host code only.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+
+#include "../../include/moe_decode.h"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kGemvCtasPerSm = 4;
+constexpr int kGemvMaxCtas = 2048;
+
+size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Bytes of the stream-K partial sums for any grid of at most kGemvMaxCtas
+// CTAs: nkb contiguous cells meet at most ceil(nkb / shortest run) + 1 runs.
+size_t gemv_partials_bound(int M, int N, int K) {
+  GemvPlan p;
+  p.chunk_tokens = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
+  p.n_chunks = (M + p.chunk_tokens - 1) / p.chunk_tokens;
+  p.n_tiles = (N + 63) / 64;
+  p.nkb = K / kBlock;
+  const long long total = (long long)p.n_chunks * p.n_tiles * p.nkb;
+  // every CTA's run is at least floor(total / G) >= floor(total / kGemvMaxCtas) cells long
+  const long long minrun = std::max<long long>(1, total / kGemvMaxCtas);
+  p.max_segs = (int)std::min<long long>(p.nkb, (p.nkb + minrun - 1) / minrun + 1);
+  return gemv_partials_bytes(p);
+}
+
+struct Layout {
+  size_t hdr, tickets, gcount, ready, partials, logits, xq, xs, ids, tw, sorted, off, act;
+  size_t h, hq, hs, rows, shared, total;
+  int n_gcount, n_ready, Imax, gI;
+};
+
+void layout_for(const moe_layer_dims& d, int M, Layout& L) {
+  const int H = d.hidden, E = d.num_experts, k = d.top_k;
+  L.Imax = std::max(d.inter, d.shared_inter);
+  L.gI = L.Imax / kBlock;
+  L.n_gcount = (E + 1) * L.gI;
+  L.n_ready = E + 1;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
+  L.hdr = take(kHdrWords * sizeof(int));
+  L.tickets = take(kMaxRouterTickets * sizeof(unsigned));
+  L.gcount = take((size_t)L.n_gcount * sizeof(int));
+  L.ready = take((size_t)L.n_ready * sizeof(int));
+  L.partials = take(gemv_partials_bound(M, E, H));
+  L.logits = take((size_t)M * E * sizeof(float));
+  L.xq = take((size_t)M * H);
+  L.xs = take((size_t)M * (H / kBlock) * sizeof(float));
+  L.ids = take((size_t)M * k * sizeof(int));
+  L.tw = take((size_t)M * k * sizeof(float));
+  L.sorted = take((size_t)M * k * sizeof(int));
+  L.off = take((size_t)(E + 1) * sizeof(int));
+  L.act = take((size_t)E * sizeof(int));
+  const size_t hrows = (size_t)M * k + M;
+  L.h = take(hrows * L.Imax * sizeof(float));
+  L.hq = take(hrows * L.Imax);
+  L.hs = take(hrows * L.gI * sizeof(float));
+  L.rows = take((size_t)M * k * H * sizeof(float));
+  L.shared = take((size_t)M * H * sizeof(float));
+  L.total = o;
+}
+
+int check_dims(const moe_layer_dims* d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->hidden <= 0 || d->inter <= 0 || d->shared_inter < 0 || d->num_experts <= 0 || d->top_k <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (!std::isfinite(d->routed_scaling) || !(d->swiglu_limit > 0.f) || !(d->rms_eps >= 0.f) ||
+      !std::isfinite(d->rms_eps))
+    return MOE_ERR_INVALID_ARG;
+  if (d->hidden % kBlock || d->hidden > 16384) return MOE_ERR_UNSUPPORTED;
+  if (d->inter % kBlock || d->inter > 8192) return MOE_ERR_UNSUPPORTED;
+  if (d->shared_inter % kBlock || d->shared_inter > 8192) return MOE_ERR_UNSUPPORTED;
+  if (d->num_experts > kMaxExperts || d->num_experts % 16) return MOE_ERR_UNSUPPORTED;
+  if (d->top_k > kMaxTopK || d->top_k > d->num_experts) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int sm_count_cached(int* out) {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return MOE_ERR_CUDA;
+    cache[dev] = n;
+  }
+  *out = cache[dev];
+  return MOE_OK;
+}
+
+int gemv_grid(long long cells, int sms) {
+  return (int)std::max<long long>(1, std::min<long long>({cells, (long long)sms * kGemvCtasPerSm,
+                                                         (long long)kGemvMaxCtas}));
+}
+
+}  // namespace
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_decode_workspace_size(const moe_layer_dims* dims, int max_tokens, size_t* bytes) {
+  const int rc = check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (!bytes || max_tokens < 1) return MOE_ERR_INVALID_ARG;
+  if ((long long)max_tokens * dims->top_k > kMaxMk) return MOE_ERR_UNSUPPORTED;
+  Layout L;
+  layout_for(*dims, max_tokens, L);
+  *bytes = L.total;
+  return MOE_OK;
+}
+
+int moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  return cudaMemsetAsync(ws, 0, ws_bytes, (cudaStream_t)stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+static int layer_impl(const moe_layer_dims* dims, const moe_layer_weights* w, int M, const void* x,
+                      const void* residual, void* out, void* residual_out, int32_t* topk_ids,
+                      float* topk_w, int32_t* sorted_routes, int32_t* expert_offsets, void* workspace,
+                      size_t ws_bytes, void* stream, void* const* events) {
+  int rc = check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (!w || M < 0) return MOE_ERR_INVALID_ARG;
+  if (M == 0) return MOE_OK;
+  if ((long long)M * dims->top_k > kMaxMk) return MOE_ERR_UNSUPPORTED;
+  const bool has_shared = dims->shared_inter > 0;
+  if (!w->router_w || !w->w13 || !w->w13_s || !w->w2 || !w->w2_s || !w->norm_gain) return MOE_ERR_INVALID_ARG;
+  if (has_shared && (!w->sw13 || !w->sw13_s || !w->sw2 || !w->sw2_s)) return MOE_ERR_INVALID_ARG;
+  if (!x || !residual || !out || !residual_out || !workspace) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(w->router_w) || !aligned16(w->w13) || !aligned16(w->w2) || !aligned16(x) ||
+      !aligned16(residual) || !aligned16(out) || !aligned16(residual_out) || !aligned16(w->norm_gain) ||
+      !aligned16(workspace) || (has_shared && (!aligned16(w->sw13) || !aligned16(w->sw2))))
+    return MOE_ERR_INVALID_ARG;
+  Layout L;
+  layout_for(*dims, M, L);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  int sms = 0;
+  if ((rc = sm_count_cached(&sms)) != MOE_OK) return rc;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  const int H = dims->hidden, E = dims->num_experts, k = dims->top_k;
+
+  GemvPlan plan;
+  const int chunk = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
+  const long long cells = (long long)((M + chunk - 1) / chunk) * ((E + 63) / 64) * (H / kBlock);
+  plan_gemv(plan, M, E, H, gemv_grid(cells, sms));
+  if ((long long)plan.n_chunks * plan.n_tiles > kMaxRouterTickets) return MOE_ERR_UNSUPPORTED;
+  if (gemv_partials_bytes(plan) > gemv_partials_bound(M, E, H)) return MOE_ERR_UNSUPPORTED;
+
+  RouterArgs ra;
+  ra.x = x; ra.W = w->router_w; ra.bias = w->sel_bias; ra.E = E; ra.k = k; ra.e8m0 = dims->e8m0 ? 1 : 0;
+  ra.scaling = dims->routed_scaling;
+  ra.partials = reinterpret_cast<float*>(ws + L.partials);
+  ra.tickets = reinterpret_cast<unsigned*>(ws + L.tickets);
+  ra.logits = reinterpret_cast<float*>(ws + L.logits);
+  ra.xq = ws + L.xq;
+  ra.xs = reinterpret_cast<float*>(ws + L.xs);
+  ra.hdr = reinterpret_cast<int*>(ws + L.hdr);
+  ra.ids = reinterpret_cast<int*>(ws + L.ids);
+  ra.tw = reinterpret_cast<float*>(ws + L.tw);
+  ra.sorted = reinterpret_cast<int*>(ws + L.sorted);
+  ra.off = reinterpret_cast<int*>(ws + L.off);
+  ra.act = reinterpret_cast<int*>(ws + L.act);
+  ra.gcount = reinterpret_cast<int*>(ws + L.gcount);
+  ra.n_gcount = L.n_gcount;
+  ra.ready = reinterpret_cast<int*>(ws + L.ready);
+  ra.n_ready = L.n_ready;
+  ra.user_ids = topk_ids; ra.user_w = topk_w; ra.user_sorted = sorted_routes; ra.user_off = expert_offsets;
+  auto mark = [&](int i) {
+    return !events || cudaEventRecord((cudaEvent_t)events[i], s) == cudaSuccess;
+  };
+  if (!mark(0)) return MOE_ERR_CUDA;
+  if (launch_router(plan, ra, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!mark(1)) return MOE_ERR_CUDA;
+
+  ExpertArgs ea;
+  ea.H = H; ea.I = dims->inter; ea.Is = dims->shared_inter; ea.E = E; ea.k = k; ea.M = M; ea.Mk = M * k;
+  ea.Imax = L.Imax; ea.gI = L.gI;
+  ea.limit = dims->swiglu_limit; ea.e8m0 = dims->e8m0 ? 1 : 0;
+  ea.w13 = w->w13; ea.w13_s = w->w13_s; ea.w2 = w->w2; ea.w2_s = w->w2_s;
+  ea.sw13 = w->sw13; ea.sw13_s = w->sw13_s; ea.sw2 = w->sw2; ea.sw2_s = w->sw2_s;
+  ea.xq = ra.xq; ea.xs = ra.xs; ea.sorted = ra.sorted; ea.off = ra.off; ea.act = ra.act;
+  ea.hdr = ra.hdr; ea.gcount = ra.gcount; ea.ready = ra.ready;
+  ea.h = reinterpret_cast<float*>(ws + L.h);
+  ea.hq = ws + L.hq;
+  ea.hs = reinterpret_cast<float*>(ws + L.hs);
+  ea.rows = reinterpret_cast<float*>(ws + L.rows);
+  ea.shared_out = reinterpret_cast<float*>(ws + L.shared);
+  if (launch_experts(ea, sms, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!mark(2)) return MOE_ERR_CUDA;
+
+  NormArgs na;
+  na.x = nullptr; na.residual = residual; na.gain = w->norm_gain;
+  na.rows = ea.rows; na.route_w = ra.tw; na.shared = has_shared ? ea.shared_out : nullptr;
+  na.out = out; na.residual_out = residual_out; na.M = M; na.H = H; na.k = k; na.eps = dims->rms_eps;
+  if (launch_rmsnorm(na, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!mark(3)) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+int moe_decode_layer(const moe_layer_dims* dims, const moe_layer_weights* w, int M, const void* x,
+                     const void* residual, void* out, void* residual_out, int32_t* topk_ids,
+                     float* topk_w, int32_t* sorted_routes, int32_t* expert_offsets, void* workspace,
+                     size_t ws_bytes, void* stream) {
+  return layer_impl(dims, w, M, x, residual, out, residual_out, topk_ids, topk_w, sorted_routes,
+                    expert_offsets, workspace, ws_bytes, stream, nullptr);
+}
+
+int moe_decode_layer_traced(const moe_layer_dims* dims, const moe_layer_weights* w, int M, const void* x,
+                            const void* residual, void* out, void* residual_out, int32_t* topk_ids,
+                            float* topk_w, int32_t* sorted_routes, int32_t* expert_offsets,
+                            void* workspace, size_t ws_bytes, void* stream, void* const* events) {
+  if (!events || !events[0] || !events[1] || !events[2] || !events[3]) return MOE_ERR_INVALID_ARG;
+  return layer_impl(dims, w, M, x, residual, out, residual_out, topk_ids, topk_w, sorted_routes,
+                    expert_offsets, workspace, ws_bytes, stream, events);
+}
+
+int splitk_gemm_workspace_size(int M, int N, int K, size_t* bytes) {
+  if (!bytes || M < 1 || N < 1 || K < 1) return MOE_ERR_INVALID_ARG;
+  if (M > 256 || N % 16 || K % kBlock) return MOE_ERR_UNSUPPORTED;
+  GemvPlan p;
+  p.chunk_tokens = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
+  const size_t tickets = (size_t)((M + p.chunk_tokens - 1) / p.chunk_tokens) * ((N + 63) / 64);
+  *bytes = align_up(tickets * sizeof(unsigned)) + gemv_partials_bound(M, N, K);
+  return MOE_OK;
+}
+
+int splitk_gemm_bf16(const void* A, const void* W, void* C, int c_fp32, int M, int N, int K, float alpha,
+                     void* ws, size_t ws_bytes, void* stream) {
+  size_t need = 0;
+  int rc = splitk_gemm_workspace_size(M, N, K, &need);
+  if (rc != MOE_OK) return rc;
+  if (!A || !W || !C || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(W) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  int sms = 0;
+  if ((rc = sm_count_cached(&sms)) != MOE_OK) return rc;
+  GemvPlan plan;
+  const int chunk = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
+  const long long cells = (long long)((M + chunk - 1) / chunk) * ((N + 63) / 64) * (K / kBlock);
+  plan_gemv(plan, M, N, K, gemv_grid(cells, sms));
+  if (gemv_partials_bytes(plan) > gemv_partials_bound(M, N, K)) return MOE_ERR_UNSUPPORTED;
+  SplitKArgs a;
+  a.A = A; a.W = W; a.C = C; a.c_fp32 = c_fp32 ? 1 : 0; a.alpha = alpha;
+  const size_t tickets = align_up((size_t)plan.n_chunks * plan.n_tiles * sizeof(unsigned));
+  a.tickets = reinterpret_cast<unsigned*>(ws);
+  a.partials = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + tickets);
+  return launch_splitk(plan, a, (cudaStream_t)stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int rmsnorm_residual(const void* x, const void* residual, const void* gain, int M, int H, float eps,
+                     const float* rows, const float* route_w, int k, const float* shared, void* out,
+                     void* residual_out, void* stream) {
+  if (M < 0 || H <= 0 || !(eps >= 0.f)) return MOE_ERR_INVALID_ARG;
+  if (H % kBlock || H > 16384) return MOE_ERR_UNSUPPORTED;
+  if (!residual || !gain || !out || !residual_out) return MOE_ERR_INVALID_ARG;
+  if (rows && (!route_w || k < 1 || k > kMaxTopK)) return MOE_ERR_INVALID_ARG;
+  if ((x && !aligned16(x)) || !aligned16(residual) || !aligned16(gain) || !aligned16(out) ||
+      !aligned16(residual_out) || (rows && !aligned16(rows)) || (shared && !aligned16(shared)))
+    return MOE_ERR_INVALID_ARG;
+  if (M == 0) return MOE_OK;
+  NormArgs na;
+  na.x = x; na.residual = residual; na.gain = gain; na.rows = rows; na.route_w = route_w;
+  na.shared = shared; na.out = out; na.residual_out = residual_out; na.M = M; na.H = H;
+  na.k = rows ? k : 0; na.eps = eps;
+  return launch_rmsnorm(na, (cudaStream_t)stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_device_status(void* ws, void* stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  int st = 0;
+  if (cudaMemcpy(&st, reinterpret_cast<int*>(ws) + kHdrStatus, sizeof(int), cudaMemcpyDeviceToHost) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaMemset(reinterpret_cast<int*>(ws) + kHdrStatus, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  return st;
+}
+
+int moe_debug_set_fault(void* ws, int fault, void* stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  const int v = fault ? 1 : 0;
+  if (cudaMemcpy(reinterpret_cast<int*>(ws) + kHdrFault, &v, sizeof(int), cudaMemcpyHostToDevice) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+const char* moe_status_str(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,434 @@
+// Skinny BF16 GEMMs streamed over the whole GPU (stream-K), used twice:
+//  * splitk_gemm_bf16: Y = alpha * A . W^T, the split-K BF16 projection that
+//    the vLLM specialized-decode draft page (module docstring;
+//    SpecializedDraft.run, eh_proj) runs above two tokens;
+//  * the MoE router: fp32 logits = x . W_gate^T (decode page,
+//    LayerStages._router), fused with the activation FP8 quantisation, sigmoid
+//    top-k, the routing weights and the stable route order (LayerStages
+//    ._mega_moe: route_order, expanded_idx_to_permuted_idx).
+//
+// Design: the weight matrix is HBM-bound (2 bytes read per multiply-add per
+// token tile), so the contraction runs on warp-level bf16 MMAs fed straight
+// from 128-bit streaming loads, and the K dimension is divided over all CTAs
+// so that every SM streams the same number of bytes.  A CTA owns a contiguous
+// run of (token chunk, 64-row tile, k-block) cells; each run that covers part
+// of a tile leaves one fp32 partial, and the last CTA to finish a tile sums
+// the partials in segment order (deterministic) and applies the epilogue.
+#include <algorithm>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kThreads = 128;  // 4 warps, 16 weight rows each: 64-row tiles
+
+__device__ __forceinline__ int cta_of_cell(long long x, long long total, int G) {
+  return (int)(((x + 1) * (long long)G + total - 1) / total) - 1;
+}
+
+struct Gemv {
+  const uint8_t* A;  // bf16 [M, K] as bytes
+  const uint8_t* W;  // bf16 [N, K]
+  int M, N, K, nkb, n_tiles, n_chunks, G, max_segs;
+  long long total;
+  float* partials;
+  unsigned* tickets;
+};
+
+// acc[tt] holds rows (g, g+8) x tokens (2q, 2q+1) of token tile tt for this
+// warp's 16 rows, summed over k-blocks [kb0, kb1).
+template <int TT>
+__device__ __forceinline__ void gemv_segment(const Gemv& d, int chunk, int tile, int kb0, int kb1,
+                                             float (&acc)[TT][4]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+#pragma unroll
+  for (int t = 0; t < TT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+  const int row0 = tile * 64 + warp * 16;
+  if (row0 >= d.N) return;
+  const size_t rowb = (size_t)d.K * 2;
+  const uint8_t* w0 = d.W + (size_t)(row0 + g) * rowb + q * 16;
+  const uint8_t* w1 = w0 + 8 * rowb;
+  const uint8_t* bp[TT];
+  bool bv[TT];
+#pragma unroll
+  for (int t = 0; t < TT; ++t) {
+    int n = chunk * 8 * TT + t * 8 + g;
+    bv[t] = n < d.M;
+    bp[t] = d.A + (size_t)(bv[t] ? n : 0) * rowb + q * 16;
+  }
+  uint4 c0[4], c1[4];
+#pragma unroll
+  for (int s = 0; s < 4; ++s) {
+    c0[s] = ld_stream(w0 + (size_t)kb0 * 256 + s * 64);
+    c1[s] = ld_stream(w1 + (size_t)kb0 * 256 + s * 64);
+  }
+#pragma unroll 1
+  for (int kb = kb0; kb < kb1; ++kb) {
+    const bool more = kb + 1 < kb1;
+    uint4 n0[4], n1[4];
+    if (more) {
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        n0[s] = ld_stream(w0 + (size_t)(kb + 1) * 256 + s * 64);
+        n1[s] = ld_stream(w1 + (size_t)(kb + 1) * 256 + s * 64);
+      }
+    }
+    uint4 b[TT][4];
+#pragma unroll
+    for (int t = 0; t < TT; ++t)
+#pragma unroll
+      for (int s = 0; s < 4; ++s)
+        b[t][s] = bv[t] ? __ldg(reinterpret_cast<const uint4*>(bp[t] + (size_t)kb * 256 + s * 64))
+                        : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int t = 0; t < TT; ++t)
+#pragma unroll
+      for (int s = 0; s < 4; ++s) mma_span_bf16(acc[t], c0[s], c1[s], b[t][s]);
+    if (more) {
+#pragma unroll
+      for (int s = 0; s < 4; ++s) { c0[s] = n0[s]; c1[s] = n1[s]; }
+    }
+  }
+}
+
+// Runs this CTA's cells.  epi(token, row, value) receives every finished
+// output; on_tile() is called (by all threads, after the epilogue of a tile)
+// in the CTA that completed a (chunk, tile).
+template <int TT, class Epi, class OnTile>
+__device__ void gemv_streamk(const Gemv& d, Epi epi, OnTile on_tile) {
+  __shared__ int s_last;
+  const int c = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+  constexpr int kTileOut = 8 * TT * 64;
+  long long cur = (long long)c * d.total / d.G;
+  const long long end = (long long)(c + 1) * d.total / d.G;
+  while (cur < end) {
+    const long long ct = cur / d.nkb;
+    const int kb0 = (int)(cur % d.nkb);
+    const int kb1 = (int)min((long long)d.nkb, kb0 + (end - cur));
+    const int chunk = (int)(ct / d.n_tiles), tile = (int)(ct % d.n_tiles);
+    const int first = cta_of_cell(ct * d.nkb, d.total, d.G);
+    const int nseg = cta_of_cell(ct * d.nkb + d.nkb - 1, d.total, d.G) - first + 1;
+    const int seg = c - first;
+    float acc[TT][4];
+    gemv_segment<TT>(d, chunk, tile, kb0, kb1, acc);
+    const int rl0 = warp * 16 + g, rl1 = rl0 + 8;
+    if (nseg == 1) {
+#pragma unroll
+      for (int t = 0; t < TT; ++t) {
+        const int n0 = chunk * 8 * TT + t * 8 + 2 * q;
+        const int r0 = tile * 64 + rl0, r1 = tile * 64 + rl1;
+        if (r0 < d.N) {
+          if (n0 < d.M) { epi(n0, r0, acc[t][0]); epi(n0, r1, acc[t][2]); }
+          if (n0 + 1 < d.M) { epi(n0 + 1, r0, acc[t][1]); epi(n0 + 1, r1, acc[t][3]); }
+        }
+      }
+      __syncthreads();
+      on_tile();
+    } else {
+      float* P = d.partials + ((size_t)ct * d.max_segs + seg) * kTileOut;
+#pragma unroll
+      for (int t = 0; t < TT; ++t) {
+        const int tl0 = t * 8 + 2 * q;
+        P[tl0 * 64 + rl0] = acc[t][0];
+        P[(tl0 + 1) * 64 + rl0] = acc[t][1];
+        P[tl0 * 64 + rl1] = acc[t][2];
+        P[(tl0 + 1) * 64 + rl1] = acc[t][3];
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        __threadfence();
+        const unsigned old = atomicAdd(d.tickets + ct, 1u);
+        s_last = (old == (unsigned)(nseg - 1));
+      }
+      __syncthreads();
+      if (s_last) {
+        __threadfence();
+        const float* P0 = d.partials + (size_t)ct * d.max_segs * kTileOut;
+        for (int idx = threadIdx.x; idx < kTileOut; idx += kThreads) {
+          const int tl = idx >> 6, rl = idx & 63;
+          const int n = chunk * 8 * TT + tl, r = tile * 64 + rl;
+          if (n < d.M && r < d.N) {
+            float v = 0.f;
+            for (int s = 0; s < nseg; ++s) v += ld_l2f(P0 + (size_t)s * kTileOut + idx);
+            epi(n, r, v);
+          }
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) d.tickets[ct] = 0u;
+        on_tile();
+      }
+    }
+    cur += kb1 - kb0;
+  }
+}
+
+template <int TT>
+__global__ void __launch_bounds__(kThreads) splitk_kernel(Gemv d, void* C, int c_fp32, float alpha) {
+  auto epi = [&](int n, int r, float v) {
+    v *= alpha;
+    if (c_fp32)
+      reinterpret_cast<float*>(C)[(size_t)n * d.N + r] = v;
+    else
+      reinterpret_cast<__nv_bfloat16*>(C)[(size_t)n * d.N + r] = __float2bfloat16_rn(v);
+  };
+  gemv_streamk<TT>(d, epi, [] {});
+}
+
+// ------------------------------------------------------------------ router
+
+struct RouterDev {
+  const float* bias;
+  int E, k, e8m0, H;
+  float scaling;
+  float* logits;
+  uint8_t* xq;
+  float* xs;
+  int* hdr;
+  int* ids;
+  float* tw;
+  int* sorted;
+  int* off;
+  int* act;
+  int* gcount;
+  int n_gcount;
+  int* ready;
+  int n_ready;
+  int32_t* user_ids;
+  float* user_w;
+  int32_t* user_sorted;
+  int32_t* user_off;
+};
+
+// Sigmoid top-k of one token by one warp: lane l holds experts l, l+32, ...
+// Slots come out in descending selection value; an exact tie goes to the
+// lower expert id.  Lane j < k ends with slot j's id and unbiased score.
+__device__ __forceinline__ void warp_topk(const RouterDev& r, int t, int lane, int& my_id, float& my_s) {
+  constexpr int kPer = kMaxExperts / 32;
+  float sel[kPer], sc[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int e = lane + 32 * i;
+    if (e < r.E) {
+      const float l = ld_l2f(r.logits + (size_t)t * r.E + e);
+      const float s = 1.f / (1.f + expf(-l));
+      sc[i] = s;
+      const float v = r.bias ? s + r.bias[e] : s;
+      sel[i] = v == v ? v : -INFINITY;  // a NaN never outranks a number
+    } else {
+      sc[i] = 0.f;
+      sel[i] = -INFINITY;
+    }
+  }
+  unsigned taken = 0;
+  my_id = -1;
+  my_s = 0.f;
+  for (int j = 0; j < r.k; ++j) {
+    float bv = -INFINITY, bs = 0.f;
+    int bi = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int e = lane + 32 * i;
+      if (e < r.E && !((taken >> i) & 1u) && (sel[i] > bv || (sel[i] == bv && e < bi))) {
+        bv = sel[i]; bi = e; bs = sc[i];
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; bs = os; }
+    }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == j) { my_id = bi; my_s = bs; }
+  }
+}
+
+__device__ void router_finish(const RouterDev& r, int M) {
+  __shared__ int s_ids[kMaxMk];
+  __shared__ int s_cnt[kMaxExperts];
+  __shared__ int s_cur[kMaxExperts];
+  __shared__ int s_nact;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int k = r.k, Mk = M * k, E = r.E;
+  __threadfence();
+  for (int t = warp; t < M; t += kThreads / 32) {
+    int id;
+    float s;
+    warp_topk(r, t, lane, id, s);
+    const float sum = warp_sum(lane < k ? s : 0.f);
+    if (lane < k) {
+      const float w = s / sum * r.scaling;
+      s_ids[t * k + lane] = id;
+      r.ids[t * k + lane] = id;
+      r.tw[t * k + lane] = w;
+      if (r.user_ids) r.user_ids[t * k + lane] = id;
+      if (r.user_w) r.user_w[t * k + lane] = w;
+    }
+  }
+  for (int e = threadIdx.x; e < E; e += kThreads) s_cnt[e] = 0;
+  __syncthreads();
+  for (int i = threadIdx.x; i < Mk; i += kThreads) atomicAdd(&s_cnt[s_ids[i]], 1);
+  __syncthreads();
+  if (warp == 0) {
+    // exclusive scans of the counts and of the active flags
+    const int per = (E + 31) / 32, b0 = lane * per;
+    int cs = 0, as = 0;
+    for (int e = b0; e < min(E, b0 + per); ++e) { cs += s_cnt[e]; as += s_cnt[e] > 0; }
+    int ci = cs, ai = as;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int c2 = __shfl_up_sync(0xffffffffu, ci, o), a2 = __shfl_up_sync(0xffffffffu, ai, o);
+      if (lane >= o) { ci += c2; ai += a2; }
+    }
+    int rc = ci - cs, ra = ai - as;
+    for (int e = b0; e < min(E, b0 + per); ++e) {
+      r.off[e] = rc;
+      if (r.user_off) r.user_off[e] = rc;
+      s_cur[e] = rc;
+      if (s_cnt[e] > 0) r.act[ra++] = e;
+      rc += s_cnt[e];
+    }
+    if (lane == 31) {
+      r.off[E] = ci;
+      if (r.user_off) r.user_off[E] = ci;
+      s_nact = ai;
+    }
+    __syncwarp();
+    // stable placement, 32 routes at a time, in route order
+    for (int base = 0; base < Mk; base += 32) {
+      const int i = base + lane;
+      const int e = i < Mk ? s_ids[i] : -1 - lane;
+      const unsigned grp = __match_any_sync(0xffffffffu, e);
+      const int leader = __ffs(grp) - 1;
+      const int rank = __popc(grp & ((1u << lane) - 1u));
+      int pos = 0;
+      if (lane == leader && i < Mk) {
+        pos = s_cur[e];
+        s_cur[e] = pos + __popc(grp);
+      }
+      pos = __shfl_sync(0xffffffffu, pos, leader);
+      if (i < Mk) {
+        r.sorted[pos + rank] = i;
+        if (r.user_sorted) r.user_sorted[pos + rank] = i;
+      }
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  // reset the expert kernel's counters and this kernel's ticket
+  for (int i = threadIdx.x; i < r.n_gcount; i += kThreads) r.gcount[i] = 0;
+  for (int i = threadIdx.x; i < r.n_ready; i += kThreads) r.ready[i] = 0;
+  if (threadIdx.x == 0) {
+    r.hdr[kHdrActive] = s_nact;
+    r.hdr[kHdrQueue] = 0;
+    r.hdr[kHdrRouterTicket] = 0;
+  }
+}
+
+template <int TT>
+__global__ void __launch_bounds__(kThreads) router_kernel(Gemv d, RouterDev r) {
+  __shared__ int s_finish;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // (1) FP8 quantisation of x, per token per 128-column group
+  {
+    const int nkbH = r.H / kBlock;
+    const int groups = d.M * nkbH;
+    const uint8_t* x = d.A;
+    for (int gi = blockIdx.x * 4 + warp; gi < groups; gi += gridDim.x * 4) {
+      const int t = gi / nkbH, kb = gi % nkbH;
+      const size_t o = (size_t)t * r.H + (size_t)kb * kBlock + 4 * lane;
+      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(x + o * 2));
+      const float v0 = bf16_lo(raw.x), v1 = bf16_hi(raw.x), v2 = bf16_lo(raw.y), v3 = bf16_hi(raw.y);
+      const float amax = warp_max(fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3))));
+      const float sc = group_scale(amax, r.e8m0);
+      *reinterpret_cast<uint32_t*>(r.xq + o) =
+          f32x4_to_e4m3x4(__fdiv_rn(v0, sc), __fdiv_rn(v1, sc), __fdiv_rn(v2, sc), __fdiv_rn(v3, sc));
+      if (lane == 0) r.xs[(size_t)t * nkbH + kb] = sc;
+    }
+  }
+  // (2) logits, (3) the CTA that completes the last tile finishes the routing
+  if (threadIdx.x == 0) s_finish = 0;
+  __syncthreads();
+  const int n_ct = d.n_chunks * d.n_tiles;
+  auto epi = [&](int n, int row, float v) { r.logits[(size_t)n * r.E + row] = v; };
+  auto on_tile = [&] {
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const int old = atomicAdd(r.hdr + kHdrRouterTicket, 1);
+      if (old == n_ct - 1) s_finish = 1;
+    }
+    __syncthreads();
+  };
+  gemv_streamk<TT>(d, epi, on_tile);
+  if (s_finish) router_finish(r, d.M);
+}
+
+Gemv make_gemv(const GemvPlan& p, const void* A, const void* W, float* partials, unsigned* tickets) {
+  Gemv d;
+  d.A = reinterpret_cast<const uint8_t*>(A);
+  d.W = reinterpret_cast<const uint8_t*>(W);
+  d.M = p.M; d.N = p.N; d.K = p.K; d.nkb = p.nkb; d.n_tiles = p.n_tiles; d.n_chunks = p.n_chunks;
+  d.G = p.G; d.max_segs = p.max_segs; d.total = p.total;
+  d.partials = partials;
+  d.tickets = tickets;
+  return d;
+}
+
+}  // namespace
+
+static int cta_of_cell_host(long long x, long long total, int G) {
+  return (int)(((x + 1) * (long long)G + total - 1) / total) - 1;
+}
+
+void plan_gemv(GemvPlan& p, int M, int N, int K, int G) {
+  p.M = M; p.N = N; p.K = K;
+  p.chunk_tokens = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
+  p.n_chunks = (M + p.chunk_tokens - 1) / p.chunk_tokens;
+  p.n_tiles = (N + 63) / 64;
+  p.nkb = K / kBlock;
+  p.total = (long long)p.n_chunks * p.n_tiles * p.nkb;
+  p.G = (int)std::min<long long>(G, p.total);
+  p.max_segs = 1;
+  for (long long ct = 0; ct < (long long)p.n_chunks * p.n_tiles; ++ct) {
+    const int a = cta_of_cell_host(ct * p.nkb, p.total, p.G);
+    const int b = cta_of_cell_host(ct * p.nkb + p.nkb - 1, p.total, p.G);
+    p.max_segs = std::max(p.max_segs, b - a + 1);
+  }
+}
+
+size_t gemv_partials_bytes(const GemvPlan& p) {
+  return (size_t)p.n_chunks * p.n_tiles * p.max_segs * p.chunk_tokens * 64 * sizeof(float);
+}
+
+cudaError_t launch_splitk(const GemvPlan& p, const SplitKArgs& a, cudaStream_t s) {
+  Gemv d = make_gemv(p, a.A, a.W, a.partials, a.tickets);
+  switch (p.chunk_tokens) {
+    case 8: splitk_kernel<1><<<p.G, kThreads, 0, s>>>(d, a.C, a.c_fp32, a.alpha); break;
+    case 16: splitk_kernel<2><<<p.G, kThreads, 0, s>>>(d, a.C, a.c_fp32, a.alpha); break;
+    default: splitk_kernel<4><<<p.G, kThreads, 0, s>>>(d, a.C, a.c_fp32, a.alpha); break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router(const GemvPlan& p, const RouterArgs& a, cudaStream_t s) {
+  Gemv d = make_gemv(p, a.x, a.W, a.partials, a.tickets);
+  RouterDev r;
+  r.bias = a.bias; r.E = a.E; r.k = a.k; r.e8m0 = a.e8m0; r.H = p.K; r.scaling = a.scaling;
+  r.logits = a.logits; r.xq = a.xq; r.xs = a.xs; r.hdr = a.hdr; r.ids = a.ids; r.tw = a.tw;
+  r.sorted = a.sorted; r.off = a.off; r.act = a.act; r.gcount = a.gcount; r.n_gcount = a.n_gcount;
+  r.ready = a.ready; r.n_ready = a.n_ready; r.user_ids = a.user_ids; r.user_w = a.user_w;
+  r.user_sorted = a.user_sorted; r.user_off = a.user_off;
+  switch (p.chunk_tokens) {
+    case 8: router_kernel<1><<<p.G, kThreads, 0, s>>>(d, r); break;
+    case 16: router_kernel<2><<<p.G, kThreads, 0, s>>>(d, r); break;
+    default: router_kernel<4><<<p.G, kThreads, 0, s>>>(d, r); break;
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace moe

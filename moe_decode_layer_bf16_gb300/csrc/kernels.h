@@ -1,0 +1,105 @@
+// Internal launch interfaces between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+constexpr int kBlock = 128;  // weight scale block side / activation group length
+
+// Header words at the start of a moe_decode_layer workspace (int32 each).
+enum HdrWord {
+  kHdrStatus = 0,        // 0 or MOE_ERR_DEVICE_TIMEOUT (sticky until read)
+  kHdrFault = 1,         // test hook: withhold the first slot's ready signal
+  kHdrRouterTicket = 2,  // tiles of router logits reduced so far
+  kHdrQueue = 3,         // expert-kernel work queue head
+  kHdrActive = 4,        // number of routed experts with at least one route
+  kHdrWords = 64
+};
+constexpr int kMaxRouterTickets = 1024;
+constexpr int kMaxMk = 4096;       // M * top_k per call
+constexpr int kMaxExperts = 512;
+constexpr int kMaxTopK = 16;
+
+// Stream-K split of a skinny GEMM Y[M, N] = A[M, K] . W[N, K]^T over G CTAs.
+// Work cells are (token chunk, 64-row tile, 128-column k-block), k fastest;
+// CTA c owns cells [c*T/G, (c+1)*T/G).
+struct GemvPlan {
+  int M, N, K;
+  int chunk_tokens;  // 8, 16 or 32
+  int n_chunks, n_tiles, nkb;
+  long long total;   // cells
+  int G;             // CTAs
+  int max_segs;      // most segments that cover one (chunk, tile)
+};
+void plan_gemv(GemvPlan& p, int M, int N, int K, int G);
+size_t gemv_partials_bytes(const GemvPlan& p);
+
+struct SplitKArgs {
+  const void* A;
+  const void* W;
+  void* C;
+  int c_fp32;
+  float alpha;
+  float* partials;
+  unsigned* tickets;
+};
+cudaError_t launch_splitk(const GemvPlan& p, const SplitKArgs& a, cudaStream_t s);
+
+struct RouterArgs {
+  const void* x;       // bf16 [M, H]
+  const void* W;       // bf16 [E, H]
+  const float* bias;   // [E] or null
+  int E, k, e8m0;
+  float scaling;
+  float* partials;
+  unsigned* tickets;
+  float* logits;       // [M, E]
+  uint8_t* xq;         // [M, H]
+  float* xs;           // [M, H/128]
+  int* hdr;
+  int* ids;            // [M*k]
+  float* tw;           // [M*k]
+  int* sorted;         // [M*k]
+  int* off;            // [E+1]
+  int* act;            // [E]
+  int* gcount;         // expert-kernel counters reset here
+  int n_gcount;
+  int* ready;
+  int n_ready;
+  int32_t* user_ids;
+  float* user_w;
+  int32_t* user_sorted;
+  int32_t* user_off;
+};
+cudaError_t launch_router(const GemvPlan& p, const RouterArgs& a, cudaStream_t s);
+
+struct ExpertArgs {
+  int H, I, Is, E, k, M, Mk, Imax, gI;
+  float limit;
+  int e8m0;
+  const uint8_t* w13; const float* w13_s;
+  const uint8_t* w2;  const float* w2_s;
+  const uint8_t* sw13; const float* sw13_s;
+  const uint8_t* sw2;  const float* sw2_s;
+  const uint8_t* xq; const float* xs;
+  const int* sorted; const int* off; const int* act;
+  int* hdr; int* gcount; int* ready;
+  float* h; uint8_t* hq; float* hs;
+  float* rows; float* shared_out;
+};
+cudaError_t launch_experts(const ExpertArgs& a, int num_sms, cudaStream_t s);
+
+struct NormArgs {
+  const void* x; const void* residual; const void* gain;
+  const float* rows; const float* route_w; const float* shared;
+  void* out; void* residual_out;
+  int M, H, k;
+  float eps;
+};
+cudaError_t launch_rmsnorm(const NormArgs& a, cudaStream_t s);
+
+int device_sm_count();
+
+}  // namespace moe

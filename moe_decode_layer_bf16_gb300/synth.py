@@ -64,10 +64,21 @@ def fp8_blocks(w32: torch.Tensor, e8m0: bool):
     return codes.contiguous(), s.contiguous()
 
 
+def make_expert(dims: LayerDims, e: int, seed: int = 0, device="cpu", weight_std: float = 0.02):
+    """Routed expert e alone: (w13 codes, w13 scales, w2 codes, w2 scales)."""
+    H, I = dims.hidden, dims.inter
+    w13, w13_s = fp8_blocks(_randn((2 * I, H), seed, "w13", e, device, weight_std), dims.e8m0)
+    w2, w2_s = fp8_blocks(_randn((H, I), seed, "w2", e, device, weight_std), dims.e8m0)
+    return w13, w13_s, w2, w2_s
+
+
 def make_layer(dims: LayerDims, seed: int = 0, device="cpu", router_std=None,
                bias_std: float | None = None, zipf_s: float | None = None,
-               weight_std: float = 0.02) -> dict:
-    """All weights of one layer as torch tensors on `device`."""
+               weight_std: float = 0.02, experts=None) -> dict:
+    """All weights of one layer as torch tensors on `device`.  With `experts`
+    given, only those routed experts are drawn (the others are left as zero
+    codes with unit scales); experts=[] skips the routed experts' tensors
+    altogether (w13, w2 and their scales are then None)."""
     H, I, Is, E = dims.hidden, dims.inter, dims.shared_inter, dims.num_experts
     if router_std is None:
         router_std = 0.05 * math.sqrt(512.0 / H)
@@ -80,13 +91,16 @@ def make_layer(dims: LayerDims, seed: int = 0, device="cpu", router_std=None,
         off = -float(zipf_s) * torch.log(rank)
         off = off - off.mean()
         router[:, 0] = off.to(torch.float32).to(device)
-    w13 = torch.empty((E, 2 * I, H), dtype=torch.uint8, device=device)
-    w13_s = torch.empty((E, 2 * I // 128, H // 128), dtype=torch.float32, device=device)
-    w2 = torch.empty((E, H, I), dtype=torch.uint8, device=device)
-    w2_s = torch.empty((E, H // 128, I // 128), dtype=torch.float32, device=device)
-    for e in range(E):
-        w13[e], w13_s[e] = fp8_blocks(_randn((2 * I, H), seed, "w13", e, device, weight_std), dims.e8m0)
-        w2[e], w2_s[e] = fp8_blocks(_randn((H, I), seed, "w2", e, device, weight_std), dims.e8m0)
+    if experts is not None and len(experts) == 0:
+        w13 = w13_s = w2 = w2_s = None
+        experts = []
+    else:
+        w13 = torch.zeros((E, 2 * I, H), dtype=torch.uint8, device=device)
+        w13_s = torch.ones((E, 2 * I // 128, H // 128), dtype=torch.float32, device=device)
+        w2 = torch.zeros((E, H, I), dtype=torch.uint8, device=device)
+        w2_s = torch.ones((E, H // 128, I // 128), dtype=torch.float32, device=device)
+    for e in (range(E) if experts is None else sorted(set(int(v) for v in experts))):
+        w13[e], w13_s[e], w2[e], w2_s[e] = make_expert(dims, e, seed, device, weight_std)
     layer = dict(router_w=router.to(torch.bfloat16), w13=w13, w13_s=w13_s, w2=w2, w2_s=w2_s)
     if Is > 0:
         layer["sw13"], layer["sw13_s"] = fp8_blocks(

@@ -363,9 +363,11 @@ def moe_decode_layer(layer: Layer, x_bf16, residual_bf16, tokens=None):
         for i, r in enumerate(rs):
             rows[r] = y[i]
             h_rows[r] = h32[i]
-    w13d, w2d = layer.expert(-1)
-    ys, hs32, _, _ = expert_mlp(xq[tokens], xs[tokens], w13d, w2d, layer.swiglu_limit, layer.e8m0)
-    shared[tokens] = ys
+    if layer.sw13 is not None or getattr(layer, "has_shared", False):
+        # a layer built without a shared expert (shared_inter = 0) adds nothing here
+        w13d, w2d = layer.expert(-1)
+        ys, hs32, _, _ = expert_mlp(xq[tokens], xs[tokens], w13d, w2d, layer.swiglu_limit, layer.e8m0)
+        shared[tokens] = ys
     m = finalize(rows, w, shared)
     out, res_out = rmsnorm_residual(m[tokens], residual_bf16[tokens], layer.gain, layer.rms_eps)
     return dict(logits=logits, scores=scores, sel=sel, ids=ids, weights=w,

@@ -1,0 +1,130 @@
+"""The C ABI on the host: the library loads, exports every symbol the header
+declares, and rejects bad arguments before touching a GPU.  CPU only."""
+
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+import moe_decode_layer_bf16_gb300 as m
+from moe_decode_layer_bf16_gb300.dims import DSV3, TINY
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_decode.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not os.path.exists(m.LIB_PATH):
+        from moe_decode_layer_bf16_gb300 import build
+        build.build()
+    return m.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("moe_decode_layer", "splitk_gemm_bf16", "rmsnorm_residual"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(L):
+    for n in declared_functions():
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    assert m.moe_status_str(0) == "ok"
+    assert "timed out" in m.moe_status_str(m.MOE_ERR_DEVICE_TIMEOUT)
+
+
+def test_workspace_size_grows_with_tokens(L):
+    sizes = [m.moe_decode_workspace_size(DSV3, t) for t in (1, 8, 32, 256)]
+    assert sizes == sorted(sizes) and sizes[0] > 0
+    # routed rows (fp32) dominate: at least M*k*H*4 bytes
+    assert sizes[-1] >= 256 * 8 * 7168 * 4
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(hidden=500), m.MOE_ERR_UNSUPPORTED),
+    (dict(inter=200), m.MOE_ERR_UNSUPPORTED),
+    (dict(num_experts=600), m.MOE_ERR_UNSUPPORTED),
+    (dict(num_experts=20), m.MOE_ERR_UNSUPPORTED),
+    (dict(top_k=17), m.MOE_ERR_UNSUPPORTED),
+    (dict(top_k=0), m.MOE_ERR_INVALID_ARG),
+    (dict(rms_eps=-1.0), m.MOE_ERR_INVALID_ARG),
+    (dict(routed_scaling=math.inf), m.MOE_ERR_INVALID_ARG),
+])
+def test_bad_dims_rejected(L, bad, code):
+    with pytest.raises(m.MoeError) as e:
+        m.moe_decode_workspace_size(TINY.with_(**bad), 4)
+    assert e.value.status == code
+
+
+def test_too_many_tokens_unsupported(L):
+    with pytest.raises(m.MoeError) as e:
+        m.moe_decode_workspace_size(DSV3, 1024)
+    assert e.value.status == m.MOE_ERR_UNSUPPORTED
+
+
+def _weights(ptr=0x1000):
+    return m._Weights(*[ptr] * len(m._WEIGHT_FIELDS))
+
+
+def test_layer_rejects_before_launch(L):
+    d = m._dims(TINY)
+    fake = ctypes.c_void_p(0x10000)
+    need = m.moe_decode_workspace_size(TINY, 4)
+    # M = 0 is a no-op
+    assert L.moe_decode_layer(ctypes.byref(d), ctypes.byref(_weights()), 0, fake, fake, fake, fake,
+                              None, None, None, None, fake, need, None) == m.MOE_OK
+    # null activation pointer
+    assert L.moe_decode_layer(ctypes.byref(d), ctypes.byref(_weights()), 4, None, fake, fake, fake,
+                              None, None, None, None, fake, need, None) == m.MOE_ERR_INVALID_ARG
+    # misaligned weight
+    assert L.moe_decode_layer(ctypes.byref(d), ctypes.byref(_weights(0x1004)), 4, fake, fake, fake, fake,
+                              None, None, None, None, fake, need, None) == m.MOE_ERR_INVALID_ARG
+    # workspace too small
+    assert L.moe_decode_layer(ctypes.byref(d), ctypes.byref(_weights()), 4, fake, fake, fake, fake,
+                              None, None, None, None, fake, need - 1, None) == m.MOE_ERR_WORKSPACE_TOO_SMALL
+    # more tokens than M*k allows
+    assert L.moe_decode_layer(ctypes.byref(d), ctypes.byref(_weights()), 2000, fake, fake, fake, fake,
+                              None, None, None, None, fake, need, None) == m.MOE_ERR_UNSUPPORTED
+
+
+def test_splitk_rejects_before_launch(L):
+    fake = ctypes.c_void_p(0x10000)
+    assert L.splitk_gemm_bf16(fake, fake, fake, 0, 4, 7168, 100, 1.0, fake, 1 << 30, None) == m.MOE_ERR_UNSUPPORTED
+    assert L.splitk_gemm_bf16(fake, fake, fake, 0, 4, 7000, 14336, 1.0, fake, 1 << 30, None) == m.MOE_ERR_UNSUPPORTED
+    assert L.splitk_gemm_bf16(fake, fake, fake, 0, 300, 7168, 14336, 1.0, fake, 1 << 30, None) == m.MOE_ERR_UNSUPPORTED
+    assert L.splitk_gemm_bf16(None, fake, fake, 0, 4, 7168, 14336, 1.0, fake, 1 << 30, None) == m.MOE_ERR_INVALID_ARG
+    need = m.splitk_gemm_workspace_size(4, 7168, 14336)
+    assert L.splitk_gemm_bf16(fake, fake, fake, 0, 4, 7168, 14336, 1.0, fake, need - 1, None) == \
+        m.MOE_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_rmsnorm_rejects_before_launch(L):
+    fake = ctypes.c_void_p(0x10000)
+    assert L.rmsnorm_residual(None, fake, fake, 4, 500, 1e-6, None, None, 0, None, fake, fake, None) == \
+        m.MOE_ERR_UNSUPPORTED
+    assert L.rmsnorm_residual(None, fake, fake, 4, 512, 1e-6, fake, None, 4, None, fake, fake, None) == \
+        m.MOE_ERR_INVALID_ARG
+    assert L.rmsnorm_residual(None, None, fake, 4, 512, 1e-6, None, None, 0, None, fake, fake, None) == \
+        m.MOE_ERR_INVALID_ARG
+    assert L.rmsnorm_residual(None, fake, fake, 0, 512, 1e-6, None, None, 0, None, fake, fake, None) == m.MOE_OK
+
+
+def test_product_path_has_no_oracle_import():
+    pkg = os.path.join(ROOT, "moe_decode_layer_bf16_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"(import\s+oracle|from\s+oracle|oracle[./]|moe_oracle)", src), f

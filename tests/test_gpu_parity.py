@@ -1,0 +1,227 @@
+"""CUDA path vs the CPU oracle, element by element, through the C ABI.
+
+Routing (top-k ids, route order, expert offsets) must match exactly; the
+routing weights within 1e-5 relative; bf16 outputs within max-abs-rel 2e-2
+(|got - ref| / max(|ref|, rms(ref)), per tensor).  Inputs are seeded and
+drawn without near-ties in the routing (tests/fixtures_moe.py).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import moe_decode_layer_bf16_gb300 as m
+from moe_decode_layer_bf16_gb300 import synth
+from moe_decode_layer_bf16_gb300.dims import DSV3, TINY
+from oracle import moe_oracle as orc
+from tests.fixtures_moe import oracle_layer, tie_free_tokens, to_np
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2
+DEV = "cuda"
+
+
+class LazyLayer(orc.Layer):
+    """Oracle view of a layer whose expert weights stay on the GPU until the
+    oracle asks for one expert (the full DeepSeek-V3-shaped layer is 11 GB)."""
+
+    def __init__(self, dims, lw):
+        self._lw = lw
+        super().__init__(router_w=to_np(lw["router_w"]), sel_bias=to_np(lw["sel_bias"]), w13=None,
+                         w13_s=None, w2=None, w2_s=None, sw13=None, sw13_s=None, sw2=None, sw2_s=None,
+                         gain=to_np(lw["gain"]), top_k=dims.top_k, routed_scaling=dims.routed_scaling,
+                         swiglu_limit=dims.swiglu_limit, rms_eps=dims.rms_eps, e8m0=dims.e8m0)
+
+    def expert(self, e):
+        if e not in self._cache:
+            self._cache.clear()
+            lw = self._lw
+            if e < 0:
+                w = (to_np(lw["sw13"]), to_np(lw["sw13_s"]), to_np(lw["sw2"]), to_np(lw["sw2_s"]))
+            else:
+                w = (to_np(lw["w13"][e]), to_np(lw["w13_s"][e]), to_np(lw["w2"][e]), to_np(lw["w2_s"][e]))
+            self._cache[e] = (orc.dequant_weight(w[0], w[1]), orc.dequant_weight(w[2], w[3]))
+        return self._cache[e]
+
+
+def run_gpu(dims, lw, x, res, layer=None):
+    M, k, E = x.shape[0], dims.top_k, dims.num_experts
+    layer = layer or m.MoeDecodeLayer(dims, lw, max_tokens=M)
+    ids = torch.full((M, k), -1, dtype=torch.int32, device=DEV)
+    tw = torch.zeros((M, k), dtype=torch.float32, device=DEV)
+    sr = torch.full((M * k,), -1, dtype=torch.int32, device=DEV)
+    off = torch.full((E + 1,), -1, dtype=torch.int32, device=DEV)
+    out, ro = layer(x, res, topk_ids=ids, topk_w=tw, sorted_routes=sr, expert_offsets=off)
+    torch.cuda.synchronize()
+    assert layer.status() == m.MOE_OK
+    return dict(out=to_np(out), residual_out=to_np(ro), ids=to_np(ids), w=to_np(tw), sorted=to_np(sr),
+                off=to_np(off))
+
+
+def compare(dims, lw, x, res, L=None, tokens=None):
+    g = run_gpu(dims, lw, x, res)
+    L = L or oracle_layer(dims, lw)
+    ref = orc.moe_decode_layer(L, to_np(x), to_np(res), tokens=tokens)
+    assert np.array_equal(g["ids"], ref["ids"]), "top-k ids differ"
+    assert np.array_equal(g["sorted"], ref["sorted_routes"]), "route order differs"
+    assert np.array_equal(g["off"], ref["offsets"]), "expert offsets differ"
+    np.testing.assert_allclose(g["w"], ref["weights"], rtol=1e-5, atol=1e-7)
+    t = ref["tokens"]
+    e_out = orc.max_abs_rel(g["out"][t], ref["out"])
+    e_res = orc.max_abs_rel(g["residual_out"][t], ref["residual_out"])
+    assert e_out <= TOL and e_res <= TOL, (e_out, e_res)
+    return g, ref, e_out, e_res
+
+
+# ------------------------------------------------------------ small layers
+
+@pytest.mark.parametrize("M", [1, 4, 13, 33])
+def test_tiny_layer(M):
+    lw = synth.make_layer(TINY, seed=0, device=DEV)
+    x, res, _ = tie_free_tokens(TINY, lw, M, seed=M, device=DEV)
+    compare(TINY, lw, x, res)
+
+
+VARIANTS = {
+    "e8m0_bias": (TINY.with_(e8m0=True), dict(bias_std=0.5), False),
+    "zipf_e64_k6": (TINY.with_(num_experts=64, top_k=6, hidden=1024), dict(zipf_s=1.1), True),
+    "no_shared": (TINY.with_(shared_inter=0), {}, False),
+    "shared_wider": (TINY.with_(inter=128, shared_inter=384), {}, False),
+    "all_experts": (TINY.with_(num_experts=16, top_k=16), {}, False),
+    "uneven_k_split": (TINY.with_(hidden=640, inter=384, shared_inter=128), {}, False),
+    "unclamped": (TINY.with_(swiglu_limit=float("inf")), {}, False),
+}
+
+
+@pytest.mark.parametrize("name", sorted(VARIANTS))
+@pytest.mark.parametrize("M", [1, 19])
+def test_layer_variants(name, M):
+    dims, kw, zipf = VARIANTS[name]
+    lw = synth.make_layer(dims, seed=7, device=DEV, **kw)
+    x, res, _ = tie_free_tokens(dims, lw, M, seed=100 + M, zipf=zipf, device=DEV)
+    compare(dims, lw, x, res)
+
+
+def test_outputs_are_deterministic():
+    dims = TINY.with_(num_experts=64, top_k=8, hidden=1024)
+    lw = synth.make_layer(dims, seed=3, device=DEV)
+    x, res, _ = tie_free_tokens(dims, lw, 40, seed=3, device=DEV)
+    layer = m.MoeDecodeLayer(dims, lw, max_tokens=40)
+    a = run_gpu(dims, lw, x, res, layer)
+    b = run_gpu(dims, lw, x, res, layer)
+    for key in a:
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_workspace_reuse_across_token_counts():
+    # one workspace sized for 33 tokens serves calls of 33, 1 and 7 tokens
+    lw = synth.make_layer(TINY, seed=5, device=DEV)
+    layer = m.MoeDecodeLayer(TINY, lw, max_tokens=33)
+    L = oracle_layer(TINY, lw)
+    for M in (33, 1, 7):
+        x, res, _ = tie_free_tokens(TINY, lw, M, seed=50 + M, device=DEV)
+        g = run_gpu(TINY, lw, x, res, layer)
+        ref = orc.moe_decode_layer(L, to_np(x), to_np(res))
+        assert np.array_equal(g["ids"], ref["ids"])
+        assert orc.max_abs_rel(g["out"], ref["out"]) <= TOL
+
+
+def test_timeout_is_reported_and_gpu_stays_usable():
+    lw = synth.make_layer(TINY, seed=1, device=DEV)
+    x, res, _ = tie_free_tokens(TINY, lw, 4, seed=1, device=DEV)
+    layer = m.MoeDecodeLayer(TINY, lw, max_tokens=4)
+    m.moe_debug_set_fault(layer.workspace, 1)
+    layer(x, res)
+    assert layer.status() == m.MOE_ERR_DEVICE_TIMEOUT
+    m.moe_debug_set_fault(layer.workspace, 0)
+    g = run_gpu(TINY, lw, x, res, layer)
+    ref = orc.moe_decode_layer(oracle_layer(TINY, lw), to_np(x), to_np(res))
+    assert orc.max_abs_rel(g["out"], ref["out"]) <= TOL
+
+
+# ------------------------------------------------------------ boundary alone
+
+def test_rmsnorm_residual_with_and_without_finalize():
+    M, H, k = 5, 1024, 4
+    gen = torch.Generator(device=DEV).manual_seed(11)
+    rnd = lambda *s: torch.randn(*s, generator=gen, device=DEV)
+    x = rnd(M, H).to(torch.bfloat16)
+    res = rnd(M, H).to(torch.bfloat16)
+    gain = (1 + 0.1 * rnd(H)).to(torch.bfloat16)
+    rows = rnd(M * k, H)
+    w = rnd(M, k).abs()
+    shared = rnd(M, H)
+    out = torch.empty_like(res)
+    ro = torch.empty_like(res)
+    # x only
+    m.rmsnorm_residual(res, gain, out, ro, 1e-6, x=x)
+    torch.cuda.synchronize()
+    ref_o, ref_r = orc.rmsnorm_residual(to_np(x), to_np(res), to_np(gain), 1e-6)
+    assert orc.max_abs_rel(to_np(out), ref_o) <= TOL and np.array_equal(to_np(ro), ref_r)
+    # finalize of rows + shared
+    m.rmsnorm_residual(res, gain, out, ro, 1e-6, rows=rows, route_w=w, shared=shared)
+    torch.cuda.synchronize()
+    mm = orc.finalize(to_np(rows).astype(np.float64), to_np(w).astype(np.float64), to_np(shared))
+    ref_o, ref_r = orc.rmsnorm_residual(mm, to_np(res), to_np(gain), 1e-6)
+    assert orc.max_abs_rel(to_np(out), ref_o) <= TOL
+    assert orc.max_abs_rel(to_np(ro), ref_r) <= 1e-2
+
+
+# ------------------------------------------------------------ split-K GEMM
+
+@pytest.mark.parametrize("M", [1, 2, 4, 8, 16])
+def test_splitk_eh_proj(M):
+    N, K = 7168, 14336
+    a, w = synth.make_projection(M, N, K, seed=M, device=DEV)
+    c = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    ws = torch.zeros(m.splitk_gemm_workspace_size(M, N, K), dtype=torch.uint8, device=DEV)
+    m.splitk_gemm_bf16(a, w, c, ws)
+    torch.cuda.synchronize()
+    ref = orc.projection(to_np(a), to_np(w))
+    assert orc.max_abs_rel(to_np(c), ref) <= 1e-2
+    # fp32 sums rounded once to bf16: at most one bf16 ulp from the float64 result
+    got = to_np(c)
+    ulp = np.abs(ref) * 2.0 ** -7 + 1e-30
+    assert (np.abs(got - ref) <= ulp).mean() > 0.999
+
+
+@pytest.mark.parametrize("M", [1, 8, 16, 33])
+def test_splitk_router_form_fp32(M):
+    N, K = 256, 7168
+    a, w = synth.make_projection(M, N, K, seed=40 + M, device=DEV)
+    c = torch.empty((M, N), dtype=torch.float32, device=DEV)
+    ws = torch.zeros(m.splitk_gemm_workspace_size(M, N, K), dtype=torch.uint8, device=DEV)
+    m.splitk_gemm_bf16(a, w, c, ws, alpha=0.5)
+    torch.cuda.synchronize()
+    ref = orc.projection(to_np(a), to_np(w), alpha=0.5, out_fp32=True)
+    assert orc.max_abs_rel(to_np(c), ref) <= 1e-4
+
+
+# ------------------------------------------------------------ full-size layers
+
+@pytest.fixture(scope="module")
+def dsv3():
+    lw = synth.make_layer(DSV3, seed=0, device=DEV)
+    return lw, LazyLayer(DSV3, lw)
+
+
+@pytest.fixture(scope="module")
+def dsv3_skewed():
+    dims = DSV3.with_(e8m0=True)
+    lw = synth.make_layer(dims, seed=4, device=DEV, bias_std=0.5, zipf_s=1.1)
+    return dims, lw, LazyLayer(dims, lw)
+
+
+@pytest.mark.parametrize("M", [1, 8, 32, 64, 128, 256])
+def test_dsv3_layer_sampled(dsv3, M):
+    lw, L = dsv3
+    x, res, _ = tie_free_tokens(DSV3, lw, M, seed=1000 + M, device=DEV)
+    tokens = sorted({0, M - 1})
+    compare(DSV3, lw, x, res, L=L, tokens=tokens)
+
+
+@pytest.mark.parametrize("M", [1, 16, 128])
+def test_dsv3_skewed_e8m0_sampled(dsv3_skewed, M):
+    dims, lw, L = dsv3_skewed
+    x, res, _ = tie_free_tokens(dims, lw, M, seed=2000 + M, zipf=True, device=DEV)
+    compare(dims, lw, x, res, L=L, tokens=sorted({0, M - 1}))
