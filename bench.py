@@ -197,7 +197,8 @@ def run_ours(args, world, rank, local):
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    dims = DSV3
+    dims = DSV3.with_(num_experts=args.num_experts)
+    MS = tuple(args.ms)
     lw = synth.make_layer(dims, seed=0, device=dev)
     layer = m.MoeDecodeLayer(dims, lw, max_tokens=max(MS), device=dev)
     inputs = {M: synth.make_tokens(M, dims.hidden, seed=100 + M, device=dev) for M in MS}
@@ -297,12 +298,14 @@ def run_ours(args, world, rank, local):
         dt, desc = oracle_sample(seed=0)
         cpu = {"value": 1.0 / dt, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
 
+    workload = WORKLOAD if (dims.num_experts == DSV3.num_experts and MS == (1, 8, 32)) else (
+        f"profiling case: H=7168 E={dims.num_experts} k=8 I=Is=2048, M in {set(MS)}")
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8",
         "data": "synthetic (seeded random-init weights and tokens)",
-        "config": {"workload": WORKLOAD, "tokens_per_step": sum(MS), "l2": "flushed (512 MB write) before every layer call",
+        "config": {"workload": workload, "tokens_per_step": sum(MS), "l2": "flushed (512 MB write) before every layer call",
                    "weights": "fp8-e4m3 with fp32 128x128 block scales; router bf16; activations bf16 in/out",
                    "parallelism": "replicas" if world > 1 else "single GPU", "per_m": per_m,
                    "wall_s_timed": round(wall, 4)},
@@ -326,6 +329,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    # profiling aids (smaller resident layer for multi-pass ncu captures)
+    ap.add_argument("--num-experts", type=int, default=DSV3.num_experts)
+    ap.add_argument("--ms", type=int, nargs="+", default=list(MS))
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":

@@ -150,6 +150,9 @@ def moe_decode_layer_traced(dims: LayerDims, weights: dict, x, residual, out, re
     three kernels (before router, before experts, before boundary, after)."""
     w = _Weights(*[_ptr(weights.get(n, weights.get("gain") if n == "norm_gain" else None))
                    for n in _WEIGHT_FIELDS])
+    for e in events:
+        if not e.cuda_event:  # torch creates the CUDA event at its first record
+            e.record()
     ev = (_vp * 4)(*[e.cuda_event for e in events])
     M = int(x.shape[0])
     rc = lib().moe_decode_layer_traced(ctypes.byref(_dims(dims)), ctypes.byref(w), M, _ptr(x),

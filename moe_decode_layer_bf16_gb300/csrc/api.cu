@@ -36,13 +36,14 @@ size_t gemv_partials_bound(int M, int N, int K) {
 struct Layout {
   size_t hdr, tickets, gcount, ready, partials, logits, xq, xs, ids, tw, sorted, off, act;
   size_t h, hq, hs, rows, shared, total;
-  int n_gcount, n_ready, Imax, gI;
+  int n_gcount, n_ready, Imax, gI, hsS;
 };
 
 void layout_for(const moe_layer_dims& d, int M, Layout& L) {
   const int H = d.hidden, E = d.num_experts, k = d.top_k;
   L.Imax = std::max(d.inter, d.shared_inter);
   L.gI = L.Imax / kBlock;
+  L.hsS = (L.gI + 31) / 32 * 32;
   L.n_gcount = (E + 1) * L.gI;
   L.n_ready = E + 1;
   size_t o = 0;
@@ -63,7 +64,7 @@ void layout_for(const moe_layer_dims& d, int M, Layout& L) {
   const size_t hrows = (size_t)M * k + M;
   L.h = take(hrows * L.Imax * sizeof(float));
   L.hq = take(hrows * L.Imax);
-  L.hs = take(hrows * L.gI * sizeof(float));
+  L.hs = take(hrows * L.hsS * sizeof(float));
   L.rows = take((size_t)M * k * H * sizeof(float));
   L.shared = take((size_t)M * H * sizeof(float));
   L.total = o;
@@ -156,7 +157,8 @@ static int layer_impl(const moe_layer_dims* dims, const moe_layer_weights* w, in
   GemvPlan plan;
   const int chunk = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
   const long long cells = (long long)((M + chunk - 1) / chunk) * ((E + 63) / 64) * (H / kBlock);
-  plan_gemv(plan, M, E, H, gemv_grid(cells, sms));
+  // at least 4 k-blocks per CTA: a tile then has at most ~nkb/4 + 1 partial sums to add
+  plan_gemv(plan, M, E, H, gemv_grid((cells + 3) / 4, sms));
   if ((long long)plan.n_chunks * plan.n_tiles > kMaxRouterTickets) return MOE_ERR_UNSUPPORTED;
   if (gemv_partials_bytes(plan) > gemv_partials_bound(M, E, H)) return MOE_ERR_UNSUPPORTED;
 
@@ -188,7 +190,7 @@ static int layer_impl(const moe_layer_dims* dims, const moe_layer_weights* w, in
 
   ExpertArgs ea;
   ea.H = H; ea.I = dims->inter; ea.Is = dims->shared_inter; ea.E = E; ea.k = k; ea.M = M; ea.Mk = M * k;
-  ea.Imax = L.Imax; ea.gI = L.gI;
+  ea.Imax = L.Imax; ea.gI = L.gI; ea.hsS = L.hsS;
   ea.limit = dims->swiglu_limit; ea.e8m0 = dims->e8m0 ? 1 : 0;
   ea.w13 = w->w13; ea.w13_s = w->w13_s; ea.w2 = w->w2; ea.w2_s = w->w2_s;
   ea.sw13 = w->sw13; ea.sw13_s = w->sw13_s; ea.sw2 = w->sw2; ea.sw2_s = w->sw2_s;

@@ -1,8 +1,8 @@
 // The routed + shared experts of one MoE decode step as one persistent kernel
 // (the decode page, vllm.models.glm5next.nvidia.specialized_decode.runtime
 // .decode, LayerStages._mega_moe: "routed experts as one kernel"; its grouped
-// form "runs the shared expert as one more expert", which is what this kernel
-// does at every token count).
+// form "runs the shared expert as one more expert", which this kernel does at
+// every token count).
 //
 // Per expert: [g; u] = xq . w13^T with 128x128 block scales, clamped SwiGLU
 // h = silu(min(g, L)) * clamp(u, -L, L), h re-quantised to FP8 per route per
@@ -10,24 +10,33 @@
 // expanded route order (the page's UnfinalizedMoEOutput rows with the
 // identity expanded->permuted map); the shared expert's output separately.
 //
-// Work: the decode step streams each active expert's FP8 weights exactly once
-// and is HBM-bound at every token count this layer sees, so the kernel is a
-// balanced weight stream:
-//   A items (expert, 16 intermediates): 16 gate + 16 up rows of w13 over all
-//     of H, split over the CTA's 4 warps by k-block, reduced in shared memory;
-//   B items (expert, 64 rows of w2) over all of I, one 16-row tile per warp.
-// A CTA pulls items from one queue (all A items, then all B items).  The A
-// item that completes the 8th slice of a 128-column group quantises that
-// group for every route; an expert's B items start once all of its groups are
-// quantised (a bounded wait: after ~0.2 s it records MOE_ERR_DEVICE_TIMEOUT
-// in the workspace status word and skips the item, so the kernel always ends).
-// Only items already taken by running CTAs are ever waited on, so the queue
-// cannot deadlock however many CTAs are resident.
-//
-// Each warp streams its operands through a private ring of cp.async stages
-// (16-byte copies, L1 bypassed), and the products run on warp-level FP8 MMAs
-// (m16n8k32, fp32 accumulate).  Per 128-column block the MMA sum is scaled by
-// weight scale x activation scale and added to fp32 accumulators.
+// The step streams each active expert's FP8 weights exactly once and is
+// HBM-bound at every token count of the workload, so the kernel is built as a
+// weight stream that never drains:
+//   * one CTA per SM, one producer warp and eight consumer warps;
+//   * work items, taken by the producer from one atomic queue (all w13 items,
+//     shared expert first, then all w2 items):
+//       A item (expert, 16 intermediates): 16 gate + 16 up rows of w13 over H,
+//       B item (expert, 128 rows of w2, one scale block) over I, streamed as
+//       four 32-row groups;
+//   * a stage is one 16 KB TMA tile of weights (4 k-blocks of 128 columns,
+//     128-byte swizzle) plus, per token of the pass, the matching 512 bytes of
+//     its FP8 activation row (1-D bulk copies), all completing on the stage's
+//     mbarrier; the producer runs up to a whole ring of stages ahead, across
+//     item boundaries, so epilogues overlap the stream;
+//   * each consumer warp takes one 16-row tile of one k-block of every stage
+//     (warp-level FP8 MMA, m16n8k32, fp32 accumulate, block scales applied per
+//     k-block); the four k-block partial sums of a tile are added in shared
+//     memory at the end of each 32-row group.
+// The A item that completes the 8th slice of a 128-column group quantises that
+// group of h for every route; an expert's B items are issued once all of its
+// groups are quantised.  Every wait is bounded (~0.2 s): on expiry the kernel
+// records MOE_ERR_DEVICE_TIMEOUT in the workspace status word, skips the work
+// and still ends, after its own copies in flight have landed.  Only items
+// already taken by running CTAs are ever waited on, so the queue cannot
+// deadlock however many CTAs are resident.
+#include <cuda.h>
+
 #include <algorithm>
 
 #include "common.cuh"
@@ -38,365 +47,228 @@ namespace moe {
 
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kThreads = kWarps * 32;
-constexpr int kNST = 3;            // cp.async stages per warp
-constexpr int kSliceA = 16;        // intermediates per A item
-constexpr int kRowsB = 64;         // w2 rows per B item
+constexpr int kKBS = 8;                   // k-blocks per stage (two TMA boxes of 4)
+constexpr int kKH = 4;                    // k-blocks per TMA box
+constexpr int kCW = 8;                    // consumer warps: one per (16-row tile, k-block pair) of a stage
+constexpr int kThreads = (kCW + 1) * 32;  // + one producer warp
+constexpr int kSliceA = 16;               // intermediates per A item
+constexpr int kRowsB = 128;               // w2 rows per B item (one scale block)
+constexpr int kRowsQ = 32;                // w2 rows per stage (a quarter of a B item)
+constexpr int kWBytes = 32768;            // weight tile per stage (two 16 KB boxes)
+constexpr int kWHalf = 16384;
+constexpr int kXStride = 1088;            // gathered activation row pitch in a stage (1024 + 64)
+constexpr int kSmemMax = 227 * 1024;
 constexpr unsigned long long kWaitNs = 200ull * 1000ull * 1000ull;
+
+// kFirst: first stage of a pass (scales are loaded); kLast: last stage of a
+// 32-row group (its epilogue runs); kPassEnd: last stage of the pass.
+// kXT: the stage's activation rows came as one TMA tile (swizzled), otherwise
+// as one bulk copy per token (rows at a 576-byte pitch).
+enum MetaFlag { kFirst = 1, kLast = 2, kSkip = 4, kEnd = 8, kPassEnd = 16, kXT = 32 };
 
 template <int TT>
 struct Cfg {
-  static constexpr int kTok = 8 * TT;                // tokens per pass
-  static constexpr int kStageW = 8 * 512;            // 8 chunks of 16 B per lane
-  static constexpr int kStage = kStageW + 2 * TT * 512;
-  static constexpr int kRingWarp = kNST * kStage;
-  static constexpr int kRing = kWarps * kRingWarp;
+  static constexpr int kTok = 8 * TT;
+  static constexpr int kXBytes = ((kTok * kXStride + 1023) / 1024) * 1024;
+  static constexpr int kXHalf = kTok * kKH * 128;  // one activation box (tokens x 4 k-blocks)
+  static constexpr int kSBytes = ((kKBS * (2 + kTok) * 4 + 1023) / 1024) * 1024;  // block scales [kKBS][2 + kTok]
+  static constexpr int kSlot = kWBytes + kXBytes + kSBytes;
+  static constexpr int kNSTMax = 4;
 };
 
-MOE_DEV void cp_async16(void* smem, const void* gmem, bool valid) {
-  const unsigned s = (unsigned)__cvta_generic_to_shared(smem);
-  const int n = valid ? 16 : 0;
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(n) : "memory");
+// ------------------------------------------------------------- PTX wrappers
+MOE_DEV uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+MOE_DEV void mbar_init(uint64_t* b, int count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
 }
-MOE_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-MOE_DEV void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+MOE_DEV void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
+}
+MOE_DEV void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
+}
+MOE_DEV bool mbar_try_wait(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok) : "r"(su32(b)), "r"(parity) : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of `parity` to complete; false (and the status
+// word set) when it did not within kWaitNs or when another wait already failed.
+MOE_DEV bool mbar_wait(uint64_t* b, uint32_t parity, int* status) {
+  if (mbar_try_wait(b, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (long it = 1; it < (1l << 26); ++it) {
+    if (mbar_try_wait(b, parity)) return true;
+    if ((it & 63) == 0) {
+      if (*(volatile int*)status != 0) return false;
+      if (globaltimer_ns() - t0 > kWaitNs) break;
+    }
+  }
+  atomicExch(status, MOE_ERR_DEVICE_TIMEOUT);
+  return false;
+}
+MOE_DEV void tma_load_5d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3, int c4,
+                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(su32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3), "r"(c4), "r"(su32(bar))
+      : "memory");
+}
+MOE_DEV void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(su32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(su32(bar))
+      : "memory");
+}
+MOE_DEV void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(su32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(su32(bar))
+      : "memory");
+}
+MOE_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(su32(dst)),
+      "l"(src), "r"(bytes), "r"(su32(bar))
+      : "memory");
+}
+MOE_DEV uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+// 16-byte chunk `c` of 128-byte row `f` of a tile written by TMA with the
+// 128-byte swizzle (chunk index XOR row index mod 8, rows 1024-byte aligned).
+MOE_DEV uint32_t swz(uint32_t base, int f, int c) { return base + f * 128 + ((c ^ (f & 7)) << 4); }
 
+// ------------------------------------------------------------- work items
 struct Slot {
-  const uint8_t* w13; const float* s13;
-  const uint8_t* w2; const float* s2;
   int Ie;      // intermediate size of this expert
   int nt;      // routes (tokens) of this expert
   int o;       // first position in the sorted route list (routed)
   int hbase;   // first h row
-  bool shared;
+  int e;       // routed expert id (-1: shared)
 };
 
-struct Smem {
-  int* off;     // [E+1]
-  int* act;     // [E]
-  int* sorted;  // [Mk]
-  float* sc;    // activation scales of a pass [kTok][nkb]
-  float* sw;    // weight scales [2][nkb]
-  uint8_t* ring;
+struct Tables {
+  const int* off;
+  const int* act;
+  const int* sorted;
 };
 
-MOE_DEV int token_of(const ExpertArgs& p, const Smem& sm, const Slot& s, int i) {
-  return s.shared ? i : sm.sorted[s.o + i] / p.k;
+struct Item {
+  bool a;
+  int slot, idx;  // slice (A) or 128-row block (B)
+};
+
+MOE_DEV Item decode_item(int item, int nA_sh, int nA_r, int totA, int nB, bool has_shared) {
+  Item it;
+  if (item < totA) {
+    it.a = true;
+    if (item < nA_sh) { it.slot = 0; it.idx = item; }
+    else { const int j = item - nA_sh; it.slot = j / nA_r + (has_shared ? 1 : 0); it.idx = j % nA_r; }
+  } else {
+    it.a = false;
+    const int j = item - totA;
+    it.slot = j / nB;
+    it.idx = j % nB;
+  }
+  return it;
 }
 
-MOE_DEV Slot make_slot(const ExpertArgs& p, const Smem& sm, int slot, bool has_shared) {
+MOE_DEV Slot make_slot(const ExpertArgs& p, const Tables& t, int slot, bool has_shared) {
   Slot s;
   if (has_shared && slot == 0) {
-    s.w13 = p.sw13; s.s13 = p.sw13_s; s.w2 = p.sw2; s.s2 = p.sw2_s;
-    s.Ie = p.Is; s.nt = p.M; s.o = 0; s.hbase = p.Mk; s.shared = true;
+    s.Ie = p.Is; s.nt = p.M; s.o = 0; s.hbase = p.Mk; s.e = -1;
   } else {
-    const int e = sm.act[slot - (has_shared ? 1 : 0)];
-    const size_t nkbH = p.H / kBlock;
-    s.w13 = p.w13 + (size_t)e * 2 * p.I * p.H;
-    s.s13 = p.w13_s + (size_t)e * (2 * p.I / kBlock) * nkbH;
-    s.w2 = p.w2 + (size_t)e * p.H * p.I;
-    s.s2 = p.w2_s + (size_t)e * nkbH * (p.I / kBlock);
-    s.Ie = p.I; s.o = sm.off[e]; s.nt = sm.off[e + 1] - s.o; s.hbase = s.o; s.shared = false;
+    s.e = t.act[slot - (has_shared ? 1 : 0)];
+    s.Ie = p.I; s.o = t.off[s.e]; s.nt = t.off[s.e + 1] - s.o; s.hbase = s.o;
   }
   return s;
 }
 
-// ------------------------------------------------------------------ A item
-template <int TT>
-__device__ void run_A(const ExpertArgs& p, const Smem& sm, const Slot& s, int slot, int sl, int fault) {
-  using C = Cfg<TT>;
-  __shared__ int s_last;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
-  const int nkb = p.H / kBlock;
-  const int kb_lo = warp * nkb / kWarps, kb_hi = (warp + 1) * nkb / kWarps, nk = kb_hi - kb_lo;
-  const size_t H = p.H;
-  const int rg = kSliceA * sl, ru = s.Ie + kSliceA * sl;
-  const uint8_t* wg0 = s.w13 + (size_t)(rg + g) * H + 16 * q;
-  const uint8_t* wg1 = wg0 + 8 * H;
-  const uint8_t* wu0 = s.w13 + (size_t)(ru + g) * H + 16 * q;
-  const uint8_t* wu1 = wu0 + 8 * H;
-  uint8_t* ring = sm.ring + warp * C::kRingWarp;
-
-  for (int p0 = 0; p0 < s.nt; p0 += C::kTok) {
-    int tokB[TT];
-#pragma unroll
-    for (int t = 0; t < TT; ++t) {
-      const int n = p0 + t * 8 + g;
-      tokB[t] = n < s.nt ? token_of(p, sm, s, n) : -1;
-    }
-    auto issue = [&](int kb, int st) {
-      uint8_t* b = ring + st * C::kStage;
-      const size_t ko = (size_t)kb * kBlock;
-      cp_async16(b + (0 * 32 + lane) * 16, wg0 + ko, true);
-      cp_async16(b + (1 * 32 + lane) * 16, wg0 + ko + 64, true);
-      cp_async16(b + (2 * 32 + lane) * 16, wg1 + ko, true);
-      cp_async16(b + (3 * 32 + lane) * 16, wg1 + ko + 64, true);
-      cp_async16(b + (4 * 32 + lane) * 16, wu0 + ko, true);
-      cp_async16(b + (5 * 32 + lane) * 16, wu0 + ko + 64, true);
-      cp_async16(b + (6 * 32 + lane) * 16, wu1 + ko, true);
-      cp_async16(b + (7 * 32 + lane) * 16, wu1 + ko + 64, true);
-      uint8_t* xb = b + C::kStageW;
-#pragma unroll
-      for (int t = 0; t < TT; ++t) {
-        const uint8_t* src = p.xq + (size_t)(tokB[t] < 0 ? 0 : tokB[t]) * H + ko + 16 * q;
-        cp_async16(xb + ((2 * t) * 32 + lane) * 16, src, tokB[t] >= 0);
-        cp_async16(xb + ((2 * t + 1) * 32 + lane) * 16, src + 64, tokB[t] >= 0);
-      }
-    };
-#pragma unroll
-    for (int i = 0; i < kNST - 1; ++i) {
-      if (i < nk) issue(kb_lo + i, i);
-      cp_async_commit();
-    }
-    // block scales of this pass: activation [kTok][nkb], weight gate/up [nkb]
-    for (int idx = tid; idx < C::kTok * nkb; idx += kThreads) {
-      const int n = p0 + idx / nkb, kb = idx % nkb;
-      sm.sc[idx] = n < s.nt ? __ldg(p.xs + (size_t)token_of(p, sm, s, n) * nkb + kb) : 0.f;
-    }
-    for (int kb = tid; kb < nkb; kb += kThreads) {
-      sm.sw[kb] = __ldg(s.s13 + (size_t)(rg / kBlock) * nkb + kb);
-      sm.sw[nkb + kb] = __ldg(s.s13 + (size_t)(ru / kBlock) * nkb + kb);
-    }
-    __syncthreads();
-
-    float ag[TT][4], au[TT][4];
-#pragma unroll
-    for (int t = 0; t < TT; ++t)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) ag[t][j] = au[t][j] = 0.f;
-
-#pragma unroll 1
-    for (int i = 0; i < nk; ++i) {
-      {
-        const int j = i + kNST - 1;
-        if (j < nk) issue(kb_lo + j, j % kNST);
-        cp_async_commit();
-      }
-      cp_async_wait<kNST - 1>();
-      const uint4* b = reinterpret_cast<const uint4*>(ring + (i % kNST) * C::kStage);
-      const uint4 g00 = b[0 * 32 + lane], g01 = b[1 * 32 + lane];
-      const uint4 g10 = b[2 * 32 + lane], g11 = b[3 * 32 + lane];
-      const uint4 u00 = b[4 * 32 + lane], u01 = b[5 * 32 + lane];
-      const uint4 u10 = b[6 * 32 + lane], u11 = b[7 * 32 + lane];
-      const int kb = kb_lo + i;
-      const float swg = sm.sw[kb], swu = sm.sw[nkb + kb];
-#pragma unroll
-      for (int t = 0; t < TT; ++t) {
-        const uint4 x0 = b[(8 + 2 * t) * 32 + lane], x1 = b[(9 + 2 * t) * 32 + lane];
-        float cg[4] = {0.f, 0.f, 0.f, 0.f}, cu[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_span_e4m3(cg, g00, g10, x0);
-        mma_span_e4m3(cg, g01, g11, x1);
-        mma_span_e4m3(cu, u00, u10, x0);
-        mma_span_e4m3(cu, u01, u11, x1);
-        const float sx0 = sm.sc[(t * 8 + 2 * q) * nkb + kb], sx1 = sm.sc[(t * 8 + 2 * q + 1) * nkb + kb];
-        const float fg0 = swg * sx0, fg1 = swg * sx1, fu0 = swu * sx0, fu1 = swu * sx1;
-        ag[t][0] += cg[0] * fg0; ag[t][1] += cg[1] * fg1; ag[t][2] += cg[2] * fg0; ag[t][3] += cg[3] * fg1;
-        au[t][0] += cu[0] * fu0; au[t][1] += cu[1] * fu1; au[t][2] += cu[2] * fu0; au[t][3] += cu[3] * fu1;
-      }
-    }
-    cp_async_wait<0>();
-    __syncthreads();
-    // cross-warp reduction over k: red[warp][row 0..31][token], rows 0..15 gate, 16..31 up
-    float* red = reinterpret_cast<float*>(sm.ring);
-    constexpr int kT = C::kTok;
-#pragma unroll
-    for (int t = 0; t < TT; ++t) {
-      const int tl = t * 8 + 2 * q;
-      float* r = red + warp * 32 * kT;
-      r[g * kT + tl] = ag[t][0];
-      r[g * kT + tl + 1] = ag[t][1];
-      r[(g + 8) * kT + tl] = ag[t][2];
-      r[(g + 8) * kT + tl + 1] = ag[t][3];
-      r[(16 + g) * kT + tl] = au[t][0];
-      r[(16 + g) * kT + tl + 1] = au[t][1];
-      r[(24 + g) * kT + tl] = au[t][2];
-      r[(24 + g) * kT + tl + 1] = au[t][3];
-    }
-    __syncthreads();
-    for (int idx = tid; idx < kSliceA * kT; idx += kThreads) {
-      const int i = idx % kSliceA, tl = idx / kSliceA, n = p0 + tl;
-      if (n < s.nt) {
-        float gs = 0.f, us = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          gs += red[w * 32 * kT + i * kT + tl];
-          us += red[w * 32 * kT + (16 + i) * kT + tl];
-        }
-        const float z = fminf(gs, p.limit);
-        const float hv = z / (1.f + expf(-z)) * fminf(fmaxf(us, -p.limit), p.limit);
-        p.h[(size_t)(s.hbase + n) * p.Imax + rg + i] = hv;
-      }
-    }
-    __syncthreads();
-  }
-
-  // the 8th finished slice of a 128-column group quantises the group
-  if (tid == 0) {
-    __threadfence();
-    const int old = atomicAdd(p.gcount + slot * p.gI + sl / (kBlock / kSliceA), 1);
-    s_last = old == kBlock / kSliceA - 1;
-  }
-  __syncthreads();
-  if (s_last) {
-    __threadfence();
-    const int grp = sl / (kBlock / kSliceA);
-    for (int n = warp; n < s.nt; n += kWarps) {
-      const size_t row = (size_t)(s.hbase + n);
-      const float4 v = ld_l2f4(p.h + row * p.Imax + grp * kBlock + 4 * lane);
-      const float amax = warp_max(fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
-      const float sc = group_scale(amax, p.e8m0);
-      *reinterpret_cast<uint32_t*>(p.hq + row * p.Imax + grp * kBlock + 4 * lane) =
-          f32x4_to_e4m3x4(__fdiv_rn(v.x, sc), __fdiv_rn(v.y, sc), __fdiv_rn(v.z, sc), __fdiv_rn(v.w, sc));
-      if (lane == 0) p.hs[row * p.gI + grp] = sc;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      if (!(fault && slot == 0)) atomicAdd(p.ready + slot, 1);
-    }
-  }
+MOE_DEV int token_of(const ExpertArgs& p, const Tables& t, const Slot& s, int i) {
+  return s.e < 0 ? i : t.sorted[s.o + i] / p.k;
 }
 
-// ------------------------------------------------------------------ B item
-template <int TT>
-__device__ void run_B(const ExpertArgs& p, const Smem& sm, const Slot& s, int slot, int rb) {
-  using C = Cfg<TT>;
-  __shared__ int s_ok;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
-  const int nkb = s.Ie / kBlock;
-  const int row0 = rb * kRowsB + warp * 16;
-  const size_t Ie = s.Ie;
-  const uint8_t* w0 = s.w2 + (size_t)(row0 + g) * Ie + 16 * q;
-  const uint8_t* w1 = w0 + 8 * Ie;
-  uint8_t* ring = sm.ring + warp * C::kRingWarp;
+struct TmaMaps {
+  CUtensorMap w13, w2, sw13, sw2;
+  CUtensorMap xq;  // x codes [M][H/128][128], box 4 k-blocks x (tokens of a pass)
+  CUtensorMap hq;  // h codes [Mk + M][Imax/128][128], same box
+};
 
-  if (tid == 0) {
-    int ok = 1;
-    if (ld_acquire(p.ready + slot) < nkb) {
-      const unsigned long long t0 = globaltimer_ns();
-      for (long it = 0;; ++it) {
-        if (ld_acquire(p.ready + slot) >= nkb) break;
-        if (*(volatile int*)(p.hdr + kHdrStatus) != 0 || it > (1l << 24)) { ok = 0; break; }
-        if (globaltimer_ns() - t0 > kWaitNs) {
-          atomicExch(p.hdr + kHdrStatus, MOE_ERR_DEVICE_TIMEOUT);
-          ok = 0;
-          break;
-        }
-        __nanosleep(128);
-      }
-    }
-    s_ok = ok;
+// Consumer-only barrier (4 warps) on an mbarrier with a bounded wait.
+struct CBar {
+  uint64_t* bar;
+  uint32_t phase;
+  int* status;
+  MOE_DEV bool sync() {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+    const bool ok = mbar_wait(bar, phase, status);
+    phase ^= 1u;
+    __syncwarp();
+    return ok;
   }
-  __syncthreads();
-  if (!s_ok) return;
+};
 
-  for (int p0 = 0; p0 < s.nt; p0 += C::kTok) {
-    int hrow[TT];
-#pragma unroll
-    for (int t = 0; t < TT; ++t) {
-      const int n = p0 + t * 8 + g;
-      hrow[t] = n < s.nt ? s.hbase + n : -1;
-    }
-    auto issue = [&](int kb, int st) {
-      uint8_t* b = ring + st * C::kStage;
-      const size_t ko = (size_t)kb * kBlock;
-      cp_async16(b + (0 * 32 + lane) * 16, w0 + ko, true);
-      cp_async16(b + (1 * 32 + lane) * 16, w0 + ko + 64, true);
-      cp_async16(b + (2 * 32 + lane) * 16, w1 + ko, true);
-      cp_async16(b + (3 * 32 + lane) * 16, w1 + ko + 64, true);
-      uint8_t* xb = b + C::kStageW;
-#pragma unroll
-      for (int t = 0; t < TT; ++t) {
-        const uint8_t* src = p.hq + (size_t)(hrow[t] < 0 ? 0 : hrow[t]) * p.Imax + ko + 16 * q;
-        cp_async16(xb + ((2 * t) * 32 + lane) * 16, src, hrow[t] >= 0);
-        cp_async16(xb + ((2 * t + 1) * 32 + lane) * 16, src + 64, hrow[t] >= 0);
-      }
-    };
-#pragma unroll
-    for (int i = 0; i < kNST - 1; ++i) {
-      if (i < nkb) issue(i, i);
-      cp_async_commit();
-    }
-    for (int idx = tid; idx < C::kTok * nkb; idx += kThreads) {
-      const int n = p0 + idx / nkb, kb = idx % nkb;
-      sm.sc[idx] = n < s.nt ? ld_l2f(p.hs + (size_t)(s.hbase + n) * p.gI + kb) : 0.f;
-    }
-    for (int kb = tid; kb < nkb; kb += kThreads)
-      sm.sw[kb] = __ldg(s.s2 + (size_t)(rb * kRowsB / kBlock) * nkb + kb);
-    __syncthreads();
-
-    float acc[TT][4];
-#pragma unroll
-    for (int t = 0; t < TT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-#pragma unroll 1
-    for (int i = 0; i < nkb; ++i) {
-      {
-        const int j = i + kNST - 1;
-        if (j < nkb) issue(j, j % kNST);
-        cp_async_commit();
-      }
-      cp_async_wait<kNST - 1>();
-      const uint4* b = reinterpret_cast<const uint4*>(ring + (i % kNST) * C::kStage);
-      const uint4 a00 = b[0 * 32 + lane], a01 = b[1 * 32 + lane];
-      const uint4 a10 = b[2 * 32 + lane], a11 = b[3 * 32 + lane];
-      const float sw = sm.sw[i];
-#pragma unroll
-      for (int t = 0; t < TT; ++t) {
-        const uint4 x0 = b[(8 + 2 * t) * 32 + lane], x1 = b[(9 + 2 * t) * 32 + lane];
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_span_e4m3(c, a00, a10, x0);
-        mma_span_e4m3(c, a01, a11, x1);
-        const float f0 = sw * sm.sc[(t * 8 + 2 * q) * nkb + i], f1 = sw * sm.sc[(t * 8 + 2 * q + 1) * nkb + i];
-        acc[t][0] += c[0] * f0; acc[t][1] += c[1] * f1; acc[t][2] += c[2] * f0; acc[t][3] += c[3] * f1;
-      }
-    }
-    cp_async_wait<0>();
-#pragma unroll
-    for (int t = 0; t < TT; ++t) {
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int n = p0 + t * 8 + 2 * q + j;
-        if (n < s.nt) {
-          float* dst = s.shared ? p.shared_out + (size_t)n * p.H
-                                : p.rows + (size_t)sm.sorted[s.o + n] * p.H;
-          dst[row0 + g] = acc[t][j];
-          dst[row0 + g + 8] = acc[t][2 + j];
-        }
-      }
-    }
-    __syncthreads();
-  }
+MOE_DEV void cp_async4(void* dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(su32(dst)), "l"(src), "r"(valid ? 4 : 0)
+               : "memory");
+}
+// Arrive on `bar` once this thread's earlier cp.async copies have landed (the
+// barrier's expected count includes this arrival).
+MOE_DEV void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(su32(bar)) : "memory");
 }
 
 template <int TT>
-__global__ void __launch_bounds__(kThreads) experts_kernel(ExpertArgs p) {
+__global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, const __grid_constant__ TmaMaps maps,
+                                                              int nst) {
   using C = Cfg<TT>;
-  extern __shared__ __align__(16) uint8_t smem[];
-  __shared__ int s_item;
-  __shared__ int s_nact;
-  const int tid = threadIdx.x;
-  const int nkbMax = max(p.H, p.Imax) / kBlock;
-  Smem sm;
-  sm.ring = smem;
-  sm.sc = reinterpret_cast<float*>(smem + C::kRing);
-  sm.sw = sm.sc + C::kTok * nkbMax;
-  sm.off = reinterpret_cast<int*>(sm.sw + 2 * nkbMax);
-  sm.act = sm.off + (p.E + 1);
-  sm.sorted = sm.act + p.E;
+  constexpr int kTok = C::kTok;
+  constexpr int kSV = 2 + kTok;  // scale values per k-block of a stage: 2 weight + kTok activation
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (su32(smem_raw) & 1023)) & 1023);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
+  const int nkbH = p.H / kBlock;
+
+  // ---- shared memory carve-up: ring slots [W tile | activation rows | scales]
+  uint8_t* ring = smem;
+  int* meta = reinterpret_cast<int*>(smem + (size_t)nst * C::kSlot);              // [nst][4]
+  uint64_t* full = reinterpret_cast<uint64_t*>(meta + 4 * nst);                    // [nst]
+  uint64_t* empty = full + nst;                                                    // [nst]
+  uint64_t* cbar_mem = empty + nst;                                                // [1]
+  float* red = reinterpret_cast<float*>(cbar_mem + 1);                             // [2][kKH][16][kTok]
+  int* s_off = reinterpret_cast<int*>(red + 2 * kKH * 16 * kTok);                  // [E+1]
+  int* s_act = s_off + (p.E + 1);                                                  // [E]
+  int* s_sorted = s_act + p.E;                                                     // [Mk]
+  int* s_misc = s_sorted + p.Mk;                                                   // [4]
+  int* s_rdy = s_misc + 4;                                                         // [E+1]
+  int* s_srow = s_rdy + (p.E + 1);                                                 // [kTok]
+  int* status = p.hdr + kHdrStatus;
 
   if (tid == 0) {
-    s_nact = *(volatile int*)(p.hdr + kHdrActive);
-    s_item = atomicAdd(p.hdr + kHdrQueue, 1);
+    for (int i = 0; i < nst; ++i) {
+      mbar_init(full + i, 1 + kKBS);  // producer's expect-tx arrival + one scale-copy arrival per k-block
+      mbar_init(empty + i, kCW);
+    }
+    mbar_init(cbar_mem, kCW);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    s_misc[0] = *(volatile int*)(p.hdr + kHdrActive);
   }
   __syncthreads();
-  const int n_act = s_nact;
-  const int fault = *(volatile int*)(p.hdr + kHdrFault);
-  for (int i = tid; i <= p.E; i += kThreads) sm.off[i] = p.off[i];
-  for (int i = tid; i < n_act; i += kThreads) sm.act[i] = p.act[i];
-  for (int i = tid; i < p.Mk; i += kThreads) sm.sorted[i] = p.sorted[i];
+  const int n_act = s_misc[0];
+  for (int i = tid; i <= p.E; i += kThreads) s_off[i] = p.off[i];
+  for (int i = tid; i < n_act; i += kThreads) s_act[i] = p.act[i];
+  for (int i = tid; i < p.Mk; i += kThreads) s_sorted[i] = p.sorted[i];
+  for (int i = tid; i <= p.E; i += kThreads) s_rdy[i] = 0;
   __syncthreads();
+  const Tables tb{s_off, s_act, s_sorted};
 
   const bool has_shared = p.Is > 0;
   const int nA_sh = has_shared ? p.Is / kSliceA : 0;
@@ -404,57 +276,407 @@ __global__ void __launch_bounds__(kThreads) experts_kernel(ExpertArgs p) {
   const int nB = p.H / kRowsB;
   const int totA = nA_sh + n_act * nA_r;
   const int total = totA + ((has_shared ? 1 : 0) + n_act) * nB;
+  const int fault = *(volatile int*)(p.hdr + kHdrFault);
 
-  int item = s_item;
-  while (item < total) {
-    __syncthreads();
-    int nxt = 0;
-    if (tid == 0) nxt = atomicAdd(p.hdr + kHdrQueue, 1);
-    if (item < totA) {
-      int slot, sl;
-      if (item < nA_sh) { slot = 0; sl = item; }
-      else { const int j = item - nA_sh; slot = j / nA_r + (has_shared ? 1 : 0); sl = j % nA_r; }
-      const Slot s = make_slot(p, sm, slot, has_shared);
-      run_A<TT>(p, sm, s, slot, sl, fault);
-    } else {
-      const int j = item - totA;
-      const int slot = j / nB, rb = j % nB;
-      const Slot s = make_slot(p, sm, slot, has_shared);
-      run_B<TT>(p, sm, s, slot, rb);
+  if (warp == kCW) {
+    // ================================================================ producer
+    // Lane 0 owns the ring and the bulk copies; all 32 lanes fetch each
+    // stage's block scales with 4-byte cp.async tracked on the stage barrier.
+    uint32_t gs = 0;
+    bool alive = true;
+    int item = 0;
+    if (lane == 0) item = atomicAdd(p.hdr + kHdrQueue, 1);
+    item = __shfl_sync(0xffffffffu, item, 0);
+    while (alive && item < total) {
+      int nxt = 0;
+      if (lane == 0) nxt = atomicAdd(p.hdr + kHdrQueue, 1);  // consumed at the end of the item
+      const Item it = decode_item(item, nA_sh, nA_r, totA, nB, has_shared);
+      const Slot s = make_slot(p, tb, it.slot, has_shared);
+      const int nkbK = it.a ? nkbH : s.Ie / kBlock;
+      const int nkg = (nkbK + kKBS - 1) / kKBS;     // k-block groups
+      const int nq = it.a ? 1 : kRowsB / kRowsQ;    // row quarters (B)
+      const int nstage = nkg * nq;
+      bool skip = false;
+      if (!it.a && !s_rdy[it.slot]) {
+        // w2 items need the expert's quantised h: wait for all its groups
+        int sk = 0;
+        if (lane == 0) {
+          if (ld_acquire(p.ready + it.slot) < nkbK) {
+            const unsigned long long t0 = globaltimer_ns();
+            for (long n = 0;; ++n) {
+              if (ld_acquire(p.ready + it.slot) >= nkbK) break;
+              if (*(volatile int*)status != 0 || n > (1l << 24)) { sk = 1; break; }
+              if (globaltimer_ns() - t0 > kWaitNs) {
+                atomicExch(status, MOE_ERR_DEVICE_TIMEOUT);
+                sk = 1;
+                break;
+              }
+              __nanosleep(64);
+            }
+          }
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          if (!sk) s_rdy[it.slot] = 1;
+        }
+        __syncwarp();  // the other lanes' scale reads come after lane 0's acquire
+        skip = __shfl_sync(0xffffffffu, sk, 0) != 0;
+      }
+      const float* w_sc = it.a ? (s.e < 0 ? p.sw13_s : p.w13_s + (size_t)s.e * (2 * p.I / kBlock) * nkbH)
+                               : (s.e < 0 ? p.sw2_s : p.w2_s + (size_t)s.e * nkbH * (p.I / kBlock));
+      const int rg = kSliceA * it.idx;
+      const int passes = skip ? 1 : (s.nt + kTok - 1) / kTok;
+      for (int pass = 0; pass < passes && alive; ++pass) {
+        const int ntok = min(kTok, s.nt - pass * kTok);
+        // activation rows: one TMA tile when the pass's rows are contiguous (w2
+        // items: h rows; the shared expert's w13 items: x rows), else one bulk
+        // copy per token, issued by lane tl
+        const bool xt = !it.a || s.e < 0;
+        const uint8_t* xsrc = nullptr;
+        if (!xt && lane < ntok) xsrc = p.xq + (size_t)token_of(p, tb, s, pass * kTok + lane) * p.H;
+        // scale source rows of the pass's tokens (x scales for w13, h scales for w2)
+        for (int tl = lane; tl < kTok; tl += 32)
+          s_srow[tl] = tl >= ntok ? -1 : (it.a ? token_of(p, tb, s, pass * kTok + tl) : s.hbase + pass * kTok + tl);
+        __syncwarp();
+        const float* xs_base = it.a ? p.xs : p.hs;
+        const int xs_stride = it.a ? nkbH : p.hsS;
+        for (int st = 0; st < (skip ? 1 : nstage); ++st) {
+          const int si = gs % nst;
+          int ok = 1;
+          if (lane == 0) ok = mbar_wait(empty + si, ((gs / nst) & 1u) ^ 1u, status);
+          __syncwarp();  // the slot is rewritten only after the consumers released it
+          if (!__shfl_sync(0xffffffffu, ok, 0)) { alive = false; break; }
+          const int qr = st / nkg, kb0 = (st - qr * nkg) * kKBS;
+          const int nkv = min(kKBS, nkbK - kb0);
+          uint8_t* wdst = ring + (size_t)si * C::kSlot;
+          uint8_t* xdst = wdst + kWBytes;
+          float* sdst = reinterpret_cast<float*>(wdst + kWBytes + C::kXBytes);
+          if (lane == 0) {
+            const int fl = skip ? kSkip
+                                : ((st == 0 ? kFirst : 0) | (st - qr * nkg == nkg - 1 ? kLast : 0) |
+                                   (st == nstage - 1 ? kPassEnd : 0) | (xt ? kXT : 0));
+            *reinterpret_cast<int4*>(meta + 4 * si) = make_int4(item, pass | (qr << 16), kb0, fl);
+            if (skip) mbar_arrive(full + si);
+            else mbar_expect_tx(full + si, kWBytes + (xt ? 2 * C::kXHalf : ntok * nkv * kBlock));
+          }
+          __syncwarp();
+          if (lane < kKBS) {
+            // block scales of k-block kb0 + lane: [w_gate/w, w_up/w, x or h of each token]
+            const int kb = kb0 + lane;
+            if (!skip && kb < nkbK) {
+              float* d = sdst + lane * kSV;
+              const float* w0 = it.a ? w_sc + (size_t)(rg / kBlock) * nkbH + kb : w_sc + (size_t)it.idx * nkbK + kb;
+              const float* w1 = it.a ? w_sc + (size_t)((s.Ie + rg) / kBlock) * nkbH + kb : w0;
+              cp_async4(d, w0, true);
+              cp_async4(d + 1, w1, true);
+              for (int tl = 0; tl < ntok; ++tl) cp_async4(d + 2 + tl, xs_base + (size_t)s_srow[tl] * xs_stride + kb, true);
+            }
+            cp_async_arrive(full + si);
+          }
+          if (!skip) {
+            if (!xt && lane < ntok)
+              bulk_load(xdst + lane * kXStride, xsrc + (size_t)kb0 * kBlock, nkv * kBlock, full + si);
+            if (lane == 0) {
+              // two boxes of 4 k-blocks each: [kb0, kb0 + 4) and [kb0 + 4, kb0 + 8)
+              for (int h = 0; h < 2; ++h) {
+                const int kh = kb0 + h * kKH;
+                uint8_t* wd = wdst + h * kWHalf;
+                uint8_t* xd = xdst + h * C::kXHalf;
+                if (it.a) {
+                  if (s.e < 0) {
+                    tma_load_5d(wd, &maps.sw13, 0, kh, rg, 0, 0, full + si);
+                    tma_load_3d(xd, &maps.xq, 0, kh, pass * kTok, full + si);
+                  } else {
+                    tma_load_5d(wd, &maps.w13, 0, kh, rg, 0, s.e, full + si);
+                  }
+                } else {
+                  const int r0 = kRowsB * it.idx + kRowsQ * qr;
+                  if (s.e < 0) tma_load_4d(wd, &maps.sw2, 0, kh, r0, 0, full + si);
+                  else tma_load_4d(wd, &maps.w2, 0, kh, r0, s.e, full + si);
+                  tma_load_3d(xd, &maps.hq, 0, kh, s.hbase + pass * kTok, full + si);
+                }
+              }
+            }
+          }
+          ++gs;
+        }
+        __syncwarp();
+      }
+      item = __shfl_sync(0xffffffffu, nxt, 0);
     }
-    if (tid == 0) s_item = nxt;
-    __syncthreads();
-    item = s_item;
+    // end marker, then make sure every copy this CTA issued has landed
+    if (alive) {
+      const int si = gs % nst;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(empty + si, ((gs / nst) & 1u) ^ 1u, status);
+      if (__shfl_sync(0xffffffffu, ok, 0)) {
+        if (lane == 0) {
+          meta[4 * si + 3] = kEnd;
+          mbar_arrive(full + si);
+        }
+        if (lane < kKBS) cp_async_arrive(full + si);
+        ++gs;
+      }
+    }
+    if (lane == 0)
+      for (uint32_t j = (gs > (uint32_t)nst ? gs - nst : 0); j < gs; ++j)
+        mbar_wait(full + (j % nst), (j / nst) & 1u, status);
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncwarp();
+  } else {
+    // ================================================================ consumers
+    CBar cb{cbar_mem, 0u, status};
+    const int tile = warp / kKH, kw = warp % kKH;  // this warp's 16-row tile; k-blocks kw and kKH + kw
+    float acc[TT][4];
+#pragma unroll
+    for (int t = 0; t < TT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+    uint32_t gs = 0;
+    int cur = -1;  // item whose description below is current
+    Item it{};
+    Slot s{};
+    int nkbK = 0;
+    while (true) {
+      const int si = gs % nst;
+      if (!mbar_wait(full + si, (gs / nst) & 1u, status)) break;
+      const int4 mt = *reinterpret_cast<const int4*>(meta + 4 * si);
+      const int item = mt.x, pass = mt.y & 0xffff, qr = mt.y >> 16, kb0 = mt.z, flags = mt.w;
+      if (flags & kEnd) break;
+      if (flags & kSkip) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty + si);
+        ++gs;
+        continue;
+      }
+      if (item != cur) {
+        cur = item;
+        it = decode_item(item, nA_sh, nA_r, totA, nB, has_shared);
+        s = make_slot(p, tb, it.slot, has_shared);
+        nkbK = it.a ? nkbH : s.Ie / kBlock;
+      }
+      const int ntok = min(kTok, s.nt - pass * kTok);
+
+      // ---- this warp's tile of its two k-blocks of the stage (one per box)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int kl = h * kKH + kw;  // k-block within the stage
+        if (kb0 + kl < nkbK) {
+          const uint32_t sb = su32(ring + (size_t)si * C::kSlot);
+          const uint32_t wb = sb + h * kWHalf;
+          const uint32_t xb = sb + kWBytes;
+          const bool xt = (flags & kXT) != 0;
+          const float* scs = reinterpret_cast<const float*>(ring + (size_t)si * C::kSlot + kWBytes + C::kXBytes) +
+                             kl * kSV;
+          // A box [gu 2][row 16][kb 4][128 B] (tile 0 gate, tile 1 up);
+          // B box [row 32][kb 4][128 B] (tile 0 rows 0..15, tile 1 rows 16..31):
+          // either way row r of tile t is 128-byte row (16 t + r) * 4 + k-block
+          uint4 a0[2], a1[2];
+#pragma unroll
+          for (int sp = 0; sp < 2; ++sp) {
+            a0[sp] = lds128(swz(wb, (tile * 16 + g) * kKH + kw, q + 4 * sp));
+            a1[sp] = lds128(swz(wb, (tile * 16 + g + 8) * kKH + kw, q + 4 * sp));
+          }
+          const float ws = scs[tile];  // A: gate / up block scale; B: the same scale twice
+#pragma unroll
+          for (int t = 0; t < TT; ++t) {
+            const int tok = t * 8 + g;
+            uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
+            if (tok < ntok) {
+              if (xt) {  // TMA box [token][kb 4][128 B], 128-byte swizzle, one per half
+                const uint32_t xh = xb + h * C::kXHalf;
+                x0 = lds128(swz(xh, tok * kKH + kw, q));
+                x1 = lds128(swz(xh, tok * kKH + kw, q + 4));
+              } else {   // one bulk row per token, 1088-byte pitch
+                x0 = lds128(xb + tok * kXStride + kl * kBlock + q * 16);
+                x1 = lds128(xb + tok * kXStride + kl * kBlock + q * 16 + 64);
+              }
+            }
+            float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_span_e4m3(c0, a0[0], a1[0], x0);
+            mma_span_e4m3(c1, a0[1], a1[1], x1);
+            // scales of tokens past the pass are not fetched: keep those columns at zero
+            const float f0 = t * 8 + 2 * q < ntok ? ws * scs[2 + t * 8 + 2 * q] : 0.f;
+            const float f1 = t * 8 + 2 * q + 1 < ntok ? ws * scs[2 + t * 8 + 2 * q + 1] : 0.f;
+            acc[t][0] += (c0[0] + c1[0]) * f0;
+            acc[t][1] += (c0[1] + c1[1]) * f1;
+            acc[t][2] += (c0[2] + c1[2]) * f0;
+            acc[t][3] += (c0[3] + c1[3]) * f1;
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + si);
+      ++gs;
+
+      if (flags & kLast) {
+        // ---- epilogue of a 32-row group: add the four k-block partial sums
+        float* r = red + (tile * kKH + kw) * 16 * kTok;
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          const int tl = t * 8 + 2 * q;
+          r[g * kTok + tl] = acc[t][0];
+          r[g * kTok + tl + 1] = acc[t][1];
+          r[(g + 8) * kTok + tl] = acc[t][2];
+          r[(g + 8) * kTok + tl + 1] = acc[t][3];
+          acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+        }
+        if (!cb.sync()) break;
+        if (it.a) {
+          const int rg = kSliceA * it.idx;
+          for (int idx = tid; idx < kSliceA * ntok; idx += kCW * 32) {
+            const int i = idx % kSliceA, tl = idx / kSliceA;
+            float gsum = 0.f, usum = 0.f;
+#pragma unroll
+            for (int w = 0; w < kKH; ++w) {
+              gsum += red[(0 * kKH + w) * 16 * kTok + i * kTok + tl];
+              usum += red[(1 * kKH + w) * 16 * kTok + i * kTok + tl];
+            }
+            const float z = fminf(gsum, p.limit);
+            const float hv = z / (1.f + expf(-z)) * fminf(fmaxf(usum, -p.limit), p.limit);
+            p.h[(size_t)(s.hbase + pass * kTok + tl) * p.Imax + rg + i] = hv;
+          }
+        } else {
+          const int row0 = kRowsB * it.idx + kRowsQ * qr;
+          for (int idx = tid; idx < kRowsQ * ntok; idx += kCW * 32) {
+            const int rr = idx % kRowsQ, tl = idx / kRowsQ, n = pass * kTok + tl;
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < kKH; ++w) v += red[((rr >> 4) * kKH + w) * 16 * kTok + (rr & 15) * kTok + tl];
+            float* dst = s.e < 0 ? p.shared_out + (size_t)n * p.H : p.rows + (size_t)tb.sorted[s.o + n] * p.H;
+            dst[row0 + rr] = v;
+          }
+        }
+        if (!cb.sync()) break;
+        if (it.a && (flags & kPassEnd) && pass * kTok + kTok >= s.nt && warp == 0) {
+          // warp 0 alone: the 8th finished slice of a 128-column group
+          // quantises the group; the other warps go on with the stream
+          int last = 0;
+          if (lane == 0) {
+            __threadfence();
+            last = atomicAdd(p.gcount + it.slot * p.gI + it.idx / (kBlock / kSliceA), 1) ==
+                   kBlock / kSliceA - 1;
+          }
+          if (__shfl_sync(0xffffffffu, last, 0)) {
+            __threadfence();
+            const int grp = it.idx / (kBlock / kSliceA);
+            constexpr int kQB = 8;  // rows whose loads are in flight together
+            for (int n0 = 0; n0 < s.nt; n0 += kQB) {
+              float4 v[kQB];
+#pragma unroll
+              for (int j = 0; j < kQB; ++j)
+                if (n0 + j < s.nt)
+                  v[j] = __ldcg(reinterpret_cast<const float4*>(p.h + (size_t)(s.hbase + n0 + j) * p.Imax +
+                                                                grp * kBlock + 4 * lane));
+#pragma unroll
+              for (int j = 0; j < kQB; ++j) {
+                if (n0 + j < s.nt) {
+                  const size_t row = (size_t)(s.hbase + n0 + j);
+                  const float amax =
+                      warp_max(fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+                  const float scl = group_scale(amax, p.e8m0);
+                  *reinterpret_cast<uint32_t*>(p.hq + row * p.Imax + grp * kBlock + 4 * lane) =
+                      f32x4_to_e4m3x4(__fdiv_rn(v[j].x, scl), __fdiv_rn(v[j].y, scl), __fdiv_rn(v[j].z, scl),
+                                      __fdiv_rn(v[j].w, scl));
+                  if (lane == 0) p.hs[row * p.hsS + grp] = scl;
+                }
+              }
+            }
+            __syncwarp();
+            if (lane == 0) {
+              __threadfence();
+              if (!(fault && it.slot == 0)) atomicAdd(p.ready + it.slot, 1);
+            }
+          }
+        }
+      }
+    }
   }
+  __syncthreads();
+}
+
+// ------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// w13 of n experts as [n][2][I][H/128][128] bytes; box = 16 rows of gate and up
+// x 4 k-blocks x 128 bytes.
+bool map_w13(CUtensorMap* m, const uint8_t* base, int H, int I, int n) {
+  const cuuint64_t dim[5] = {128, (cuuint64_t)H / 128, (cuuint64_t)I, 2, (cuuint64_t)n};
+  const cuuint64_t stride[4] = {128, (cuuint64_t)H, (cuuint64_t)I * H, (cuuint64_t)2 * I * H};
+  const cuuint32_t box[5] = {128, kKH, kSliceA, 2, 1};
+  const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<uint8_t*>(base), dim, stride, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// w2 of n experts as [n][H][I/128][128]; box = 32 rows x 4 k-blocks x 128 bytes.
+bool map_w2(CUtensorMap* m, const uint8_t* base, int H, int I, int n) {
+  const cuuint64_t dim[4] = {128, (cuuint64_t)I / 128, (cuuint64_t)H, (cuuint64_t)n};
+  const cuuint64_t stride[3] = {128, (cuuint64_t)I, (cuuint64_t)H * I};
+  const cuuint32_t box[4] = {128, kKH, kRowsQ, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t*>(base), dim, stride, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int TT>
-size_t experts_smem(const ExpertArgs& a) {
-  const int nkbMax = std::max(a.H, a.Imax) / kBlock;
-  return Cfg<TT>::kRing + sizeof(float) * (Cfg<TT>::kTok * nkbMax + 2 * nkbMax) +
-         sizeof(int) * (2 * a.E + 1 + a.Mk);
+size_t other_smem(const ExpertArgs& a, int nst) {
+  return (size_t)nst * (4 * sizeof(int) + 2 * sizeof(uint64_t)) + sizeof(uint64_t) +
+         sizeof(float) * ((size_t)2 * kKH * 16 * Cfg<TT>::kTok) +
+         sizeof(int) * (3 * a.E + 2 + a.Mk + 4 + Cfg<TT>::kTok) + 1024;
+}
+
+// activation codes [rows][K/128][128] bytes; box = 4 k-blocks x `box_rows` rows
+bool map_rows(CUtensorMap* m, const uint8_t* base, int K, int rows, int box_rows) {
+  const cuuint64_t dim[3] = {128, (cuuint64_t)K / 128, (cuuint64_t)rows};
+  const cuuint64_t stride[2] = {128, (cuuint64_t)K};
+  const cuuint32_t box[3] = {128, kKH, (cuuint32_t)box_rows};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t*>(base), dim, stride, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int TT>
-cudaError_t launch_tt(const ExpertArgs& a, int num_sms, cudaStream_t s) {
-  const size_t smem = experts_smem<TT>(a);
-  cudaError_t err = cudaFuncSetAttribute(experts_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+cudaError_t launch_tt(const ExpertArgs& a, TmaMaps& maps, int num_sms, cudaStream_t s) {
+  if (!map_rows(&maps.xq, a.xq, a.H, a.M, Cfg<TT>::kTok) || !map_rows(&maps.hq, a.hq, a.Imax, a.Mk + a.M, Cfg<TT>::kTok))
+    return cudaErrorInvalidValue;
+  int nst = Cfg<TT>::kNSTMax;
+  while (nst > 2 && (size_t)nst * Cfg<TT>::kSlot + other_smem<TT>(a, nst) > (size_t)kSmemMax) --nst;
+  const size_t smem = (size_t)nst * Cfg<TT>::kSlot + other_smem<TT>(a, nst);
+  if (smem > (size_t)kSmemMax) return cudaErrorInvalidConfiguration;
+  cudaError_t err = cudaFuncSetAttribute(experts_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  int per_sm = 0;
-  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, experts_kernel<TT>, kThreads, smem);
-  if (err != cudaSuccess) return err;
-  if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  experts_kernel<TT><<<per_sm * num_sms, kThreads, smem, s>>>(a);
+  experts_kernel<TT><<<num_sms, kThreads, smem, s>>>(a, maps, nst);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_experts(const ExpertArgs& a, int num_sms, cudaStream_t s) {
-  if (a.M <= 8) return launch_tt<1>(a, num_sms, s);
-  if (a.M <= 16) return launch_tt<2>(a, num_sms, s);
-  return launch_tt<4>(a, num_sms, s);
+  if (!encode_fn()) return cudaErrorNotSupported;
+  TmaMaps maps;
+  memset(&maps, 0, sizeof(maps));
+  if (!map_w13(&maps.w13, a.w13, a.H, a.I, a.E) || !map_w2(&maps.w2, a.w2, a.H, a.I, a.E))
+    return cudaErrorInvalidValue;
+  if (a.Is > 0 && (!map_w13(&maps.sw13, a.sw13, a.H, a.Is, 1) || !map_w2(&maps.sw2, a.sw2, a.H, a.Is, 1)))
+    return cudaErrorInvalidValue;
+  if (a.M <= 8) return launch_tt<1>(a, maps, num_sms, s);
+  if (a.M <= 16) return launch_tt<2>(a, maps, num_sms, s);
+  return launch_tt<4>(a, maps, num_sms, s);
 }
 
 }  // namespace moe

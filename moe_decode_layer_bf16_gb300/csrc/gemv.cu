@@ -148,12 +148,21 @@ __device__ void gemv_streamk(const Gemv& d, Epi epi, OnTile on_tile) {
       if (s_last) {
         __threadfence();
         const float* P0 = d.partials + (size_t)ct * d.max_segs * kTileOut;
-        for (int idx = threadIdx.x; idx < kTileOut; idx += kThreads) {
+        // only the valid tokens of the chunk; the segment loads of one output are
+        // independent and issued 8 at a time, then added in segment order
+        const int ntok = min(8 * TT, d.M - chunk * 8 * TT);
+        for (int idx = threadIdx.x; idx < ntok * 64; idx += kThreads) {
           const int tl = idx >> 6, rl = idx & 63;
           const int n = chunk * 8 * TT + tl, r = tile * 64 + rl;
-          if (n < d.M && r < d.N) {
+          if (r < d.N) {
             float v = 0.f;
-            for (int s = 0; s < nseg; ++s) v += ld_l2f(P0 + (size_t)s * kTileOut + idx);
+            for (int s = 0; s < nseg; s += 16) {
+              float t[16];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) t[j] = s + j < nseg ? __ldcg(P0 + (size_t)(s + j) * kTileOut + idx) : 0.f;
+#pragma unroll
+              for (int j = 0; j < 16; ++j) v += t[j];
+            }
             epi(n, r, v);
           }
         }
@@ -206,14 +215,15 @@ struct RouterDev {
 // Sigmoid top-k of one token by one warp: lane l holds experts l, l+32, ...
 // Slots come out in descending selection value; an exact tie goes to the
 // lower expert id.  Lane j < k ends with slot j's id and unbiased score.
-__device__ __forceinline__ void warp_topk(const RouterDev& r, int t, int lane, int& my_id, float& my_s) {
+__device__ __forceinline__ void warp_topk(const RouterDev& r, const float* logit, int lane, int& my_id,
+                                          float& my_s) {
   constexpr int kPer = kMaxExperts / 32;
   float sel[kPer], sc[kPer];
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
     const int e = lane + 32 * i;
     if (e < r.E) {
-      const float l = ld_l2f(r.logits + (size_t)t * r.E + e);
+      const float l = logit[e];
       const float s = 1.f / (1.f + expf(-l));
       sc[i] = s;
       const float v = r.bias ? s + r.bias[e] : s;
@@ -248,18 +258,27 @@ __device__ __forceinline__ void warp_topk(const RouterDev& r, int t, int lane, i
   }
 }
 
+constexpr int kTopkChunk = 8;  // tokens whose logits are staged in shared memory at once
+
 __device__ void router_finish(const RouterDev& r, int M) {
   __shared__ int s_ids[kMaxMk];
   __shared__ int s_cnt[kMaxExperts];
   __shared__ int s_cur[kMaxExperts];
+  __shared__ __align__(16) float s_logit[kTopkChunk * kMaxExperts];
   __shared__ int s_nact;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int k = r.k, Mk = M * k, E = r.E;
   __threadfence();
-  for (int t = warp; t < M; t += kThreads / 32) {
+  for (int c0 = 0; c0 < M; c0 += kTopkChunk) {
+    // one coalesced, batched load of the chunk's logits (written by other CTAs: L2)
+    const int n = min(kTopkChunk, M - c0) * E;
+    for (int i = threadIdx.x * 4; i < n; i += kThreads * 4)
+      *reinterpret_cast<float4*>(s_logit + i) = __ldcg(reinterpret_cast<const float4*>(r.logits + (size_t)c0 * E + i));
+    __syncthreads();
+    for (int t = c0 + warp; t < min(M, c0 + kTopkChunk); t += kThreads / 32) {
     int id;
     float s;
-    warp_topk(r, t, lane, id, s);
+    warp_topk(r, s_logit + (t - c0) * E, lane, id, s);
     const float sum = warp_sum(lane < k ? s : 0.f);
     if (lane < k) {
       const float w = s / sum * r.scaling;
@@ -269,6 +288,8 @@ __device__ void router_finish(const RouterDev& r, int M) {
       if (r.user_ids) r.user_ids[t * k + lane] = id;
       if (r.user_w) r.user_w[t * k + lane] = w;
     }
+    }
+    __syncthreads();
   }
   for (int e = threadIdx.x; e < E; e += kThreads) s_cnt[e] = 0;
   __syncthreads();

@@ -77,6 +77,7 @@ cudaError_t launch_router(const GemvPlan& p, const RouterArgs& a, cudaStream_t s
 
 struct ExpertArgs {
   int H, I, Is, E, k, M, Mk, Imax, gI;
+  int hsS;  // row stride (floats) of the h scales: gI rounded up to 32 (one 128-byte line per row)
   float limit;
   int e8m0;
   const uint8_t* w13; const float* w13_s;

@@ -23,7 +23,7 @@ namespace moe {
 namespace {
 
 constexpr int kCluster = 8;
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 constexpr int kMaxCols = 16384 / kCluster;
 
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
@@ -49,10 +49,21 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
       m[0] = bf16_lo(v.x); m[1] = bf16_hi(v.x); m[2] = bf16_lo(v.y); m[3] = bf16_hi(v.y);
     }
     if (a.rows) {
-      for (int s = 0; s < a.k; ++s) {
-        const float w = a.route_w[(size_t)t * a.k + s];
-        const float4 r = *reinterpret_cast<const float4*>(a.rows + ((size_t)t * a.k + s) * a.H + c0 + j);
-        m[0] += w * r.x; m[1] += w * r.y; m[2] += w * r.z; m[3] += w * r.w;
+      // all k rows are loaded before any is added, so the loads overlap
+      float w[kMaxTopK];
+      float4 r[kMaxTopK];
+#pragma unroll
+      for (int s = 0; s < kMaxTopK; ++s) {
+        if (s < a.k) {
+          w[s] = a.route_w[(size_t)t * a.k + s];
+          r[s] = *reinterpret_cast<const float4*>(a.rows + ((size_t)t * a.k + s) * a.H + c0 + j);
+        }
+      }
+#pragma unroll
+      for (int s = 0; s < kMaxTopK; ++s) {
+        if (s < a.k) {
+          m[0] += w[s] * r[s].x; m[1] += w[s] * r[s].y; m[2] += w[s] * r[s].z; m[3] += w[s] * r[s].w;
+        }
       }
     }
     if (a.shared) {

@@ -300,7 +300,8 @@ class Layer:
     gain: bf16 values as float64 [H]."""
 
     def __init__(self, *, router_w, sel_bias, w13, w13_s, w2, w2_s, sw13, sw13_s,
-                 sw2, sw2_s, gain, top_k, routed_scaling, swiglu_limit, rms_eps, e8m0):
+                 sw2, sw2_s, gain, top_k, routed_scaling, swiglu_limit, rms_eps, e8m0,
+                 has_shared=None):
         self.router_w = np.asarray(router_w, np.float64)
         self.sel_bias = None if sel_bias is None else np.asarray(sel_bias, np.float32)
         self.w13, self.w13_s, self.w2, self.w2_s = w13, w13_s, w2, w2_s
@@ -311,6 +312,8 @@ class Layer:
         self.swiglu_limit = float(swiglu_limit)
         self.rms_eps = float(rms_eps)
         self.e8m0 = bool(e8m0)
+        # a layer without a shared expert (shared_inter = 0) passes no shared weights
+        self.has_shared = (sw13 is not None) if has_shared is None else bool(has_shared)
         self._cache: dict = {}
 
     @property
@@ -363,8 +366,7 @@ def moe_decode_layer(layer: Layer, x_bf16, residual_bf16, tokens=None):
         for i, r in enumerate(rs):
             rows[r] = y[i]
             h_rows[r] = h32[i]
-    if layer.sw13 is not None or getattr(layer, "has_shared", False):
-        # a layer built without a shared expert (shared_inter = 0) adds nothing here
+    if layer.has_shared:
         w13d, w2d = layer.expert(-1)
         ys, hs32, _, _ = expert_mlp(xq[tokens], xs[tokens], w13d, w2d, layer.swiglu_limit, layer.e8m0)
         shared[tokens] = ys

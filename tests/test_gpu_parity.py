@@ -30,7 +30,8 @@ class LazyLayer(orc.Layer):
         super().__init__(router_w=to_np(lw["router_w"]), sel_bias=to_np(lw["sel_bias"]), w13=None,
                          w13_s=None, w2=None, w2_s=None, sw13=None, sw13_s=None, sw2=None, sw2_s=None,
                          gain=to_np(lw["gain"]), top_k=dims.top_k, routed_scaling=dims.routed_scaling,
-                         swiglu_limit=dims.swiglu_limit, rms_eps=dims.rms_eps, e8m0=dims.e8m0)
+                         swiglu_limit=dims.swiglu_limit, rms_eps=dims.rms_eps, e8m0=dims.e8m0,
+                         has_shared=lw["sw13"] is not None)
 
     def expert(self, e):
         if e not in self._cache:

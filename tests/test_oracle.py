@@ -273,3 +273,17 @@ def test_expert_mlp_gate_rows_then_up_rows():
     want = np.minimum(a_q, 7.0) / (1 + np.exp(-np.minimum(a_q, 7.0)))
     assert np.allclose(h32[0], want, rtol=1e-6)
     assert np.allclose(y[0], want, rtol=2.0 ** -4, atol=1e-3)
+
+
+def test_shared_expert_term_present_only_when_given():
+    # the same layer with and without its shared expert differs by exactly
+    # the shared expert's output (pre-norm sum m)
+    lw = synth.make_layer(TINY, seed=2)
+    x, res = synth.make_tokens(3, TINY.hidden, seed=2)
+    with_sh = orc.moe_decode_layer(oracle_layer(TINY, lw), to_np(x), to_np(res))
+    L = oracle_layer(TINY, lw)
+    L.has_shared = False
+    without = orc.moe_decode_layer(L, to_np(x), to_np(res))
+    sh = orc.expert_mlp(with_sh["xq"], with_sh["xs"], *L.expert(-1), L.swiglu_limit, L.e8m0)[0]
+    assert np.allclose(with_sh["m"] - without["m"], sh, rtol=1e-12, atol=1e-12)
+    assert np.abs(sh).max() > 0.1
