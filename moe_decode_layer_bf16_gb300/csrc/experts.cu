@@ -13,7 +13,8 @@
 // The step streams each active expert's FP8 weights exactly once and is
 // HBM-bound at every token count of the workload, so the kernel is built as a
 // weight stream that never drains:
-//   * one CTA per SM, one producer warp and eight consumer warps;
+//   * one CTA per SM: one producer warp, eight consumer warps and one
+//     epilogue warp;
 //   * work items, taken by the producer from one atomic queue (all w13 items,
 //     shared expert first, then all w2 items):
 //       A item (expert, 16 intermediates): 16 gate + 16 up rows of w13 over H,
@@ -50,7 +51,9 @@ namespace {
 constexpr int kKBS = 8;                   // k-blocks per stage (two TMA boxes of 4)
 constexpr int kKH = 4;                    // k-blocks per TMA box
 constexpr int kCW = 8;                    // consumer warps: one per (16-row tile, k-block pair) of a stage
-constexpr int kThreads = (kCW + 1) * 32;  // + one producer warp
+constexpr int kPW = kCW;                  // producer warp
+constexpr int kEW = kCW + 1;              // epilogue warp
+constexpr int kThreads = (kCW + 2) * 32;
 constexpr int kSliceA = 16;               // intermediates per A item
 constexpr int kRowsB = 128;               // w2 rows per B item (one scale block)
 constexpr int kRowsQ = 32;                // w2 rows per stage (a quarter of a B item)
@@ -201,21 +204,6 @@ struct TmaMaps {
   CUtensorMap hq;  // h codes [Mk + M][Imax/128][128], same box
 };
 
-// Consumer-only barrier (4 warps) on an mbarrier with a bounded wait.
-struct CBar {
-  uint64_t* bar;
-  uint32_t phase;
-  int* status;
-  MOE_DEV bool sync() {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-    const bool ok = mbar_wait(bar, phase, status);
-    phase ^= 1u;
-    __syncwarp();
-    return ok;
-  }
-};
-
 MOE_DEV void cp_async4(void* dst, const void* src, bool valid) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(su32(dst)), "l"(src), "r"(valid ? 4 : 0)
                : "memory");
@@ -224,6 +212,12 @@ MOE_DEV void cp_async4(void* dst, const void* src, bool valid) {
 // barrier's expected count includes this arrival).
 MOE_DEV void cp_async_arrive(uint64_t* bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(su32(bar)) : "memory");
+}
+
+MOE_DEV int ld_relaxed(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 
 template <int TT>
@@ -242,9 +236,11 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
   int* meta = reinterpret_cast<int*>(smem + (size_t)nst * C::kSlot);              // [nst][4]
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + 4 * nst);                    // [nst]
   uint64_t* empty = full + nst;                                                    // [nst]
-  uint64_t* cbar_mem = empty + nst;                                                // [1]
-  float* red = reinterpret_cast<float*>(cbar_mem + 1);                             // [2][kKH][16][kTok]
-  int* s_off = reinterpret_cast<int*>(red + 2 * kKH * 16 * kTok);                  // [E+1]
+  uint64_t* red_full = empty + nst;                                                // [1]
+  uint64_t* red_empty = red_full + 1;                                              // [1]
+  float* red = reinterpret_cast<float*>(red_empty + 1);                            // [2][kKH][16][kTok]
+  int* epi = reinterpret_cast<int*>(red + 2 * kKH * 16 * kTok);                    // [4]
+  int* s_off = epi + 4;                                                            // [E+1]
   int* s_act = s_off + (p.E + 1);                                                  // [E]
   int* s_sorted = s_act + p.E;                                                     // [Mk]
   int* s_misc = s_sorted + p.Mk;                                                   // [4]
@@ -257,7 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
       mbar_init(full + i, 1 + kKBS);  // producer's expect-tx arrival + one scale-copy arrival per k-block
       mbar_init(empty + i, kCW);
     }
-    mbar_init(cbar_mem, kCW);
+    mbar_init(red_full, kCW);
+    mbar_init(red_empty, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_misc[0] = *(volatile int*)(p.hdr + kHdrActive);
   }
@@ -278,18 +275,20 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
   const int total = totA + ((has_shared ? 1 : 0) + n_act) * nB;
   const int fault = *(volatile int*)(p.hdr + kHdrFault);
 
-  if (warp == kCW) {
+  if (warp == kPW) {
     // ================================================================ producer
-    // Lane 0 owns the ring and the bulk copies; all 32 lanes fetch each
-    // stage's block scales with 4-byte cp.async tracked on the stage barrier.
+    // Lane 0 owns the ring and the TMA copies; lanes 0..7 fetch each stage's
+    // block scales (one k-block each) with 4-byte cp.async on the stage barrier;
+    // lane tl copies gathered activation row tl.
     uint32_t gs = 0;
     bool alive = true;
     int item = 0;
+    int pre_slot = -1, pre_val = 0;  // lane 0: readiness of the next item's expert, loaded ahead
     if (lane == 0) item = atomicAdd(p.hdr + kHdrQueue, 1);
     item = __shfl_sync(0xffffffffu, item, 0);
     while (alive && item < total) {
       int nxt = 0;
-      if (lane == 0) nxt = atomicAdd(p.hdr + kHdrQueue, 1);  // consumed at the end of the item
+      if (lane == 0) nxt = atomicAdd(p.hdr + kHdrQueue, 1);
       const Item it = decode_item(item, nA_sh, nA_r, totA, nB, has_shared);
       const Slot s = make_slot(p, tb, it.slot, has_shared);
       const int nkbK = it.a ? nkbH : s.Ie / kBlock;
@@ -298,13 +297,13 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
       const int nstage = nkg * nq;
       bool skip = false;
       if (!it.a && !s_rdy[it.slot]) {
-        // w2 items need the expert's quantised h: wait for all its groups
+        // w2 items need the expert's quantised h: all of its groups
         int sk = 0;
         if (lane == 0) {
-          if (ld_acquire(p.ready + it.slot) < nkbK) {
+          if (!(pre_slot == it.slot && pre_val >= nkbK)) {
             const unsigned long long t0 = globaltimer_ns();
             for (long n = 0;; ++n) {
-              if (ld_acquire(p.ready + it.slot) >= nkbK) break;
+              if (ld_relaxed(p.ready + it.slot) >= nkbK) break;
               if (*(volatile int*)status != 0 || n > (1l << 24)) { sk = 1; break; }
               if (globaltimer_ns() - t0 > kWaitNs) {
                 atomicExch(status, MOE_ERR_DEVICE_TIMEOUT);
@@ -314,6 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
               __nanosleep(64);
             }
           }
+          // acquire the expert's h codes and scales, for this thread's TMA reads too
+          asm volatile("fence.acq_rel.gpu;" ::: "memory");
           asm volatile("fence.proxy.async.global;" ::: "memory");
           if (!sk) s_rdy[it.slot] = 1;
         }
@@ -326,9 +327,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
       const int passes = skip ? 1 : (s.nt + kTok - 1) / kTok;
       for (int pass = 0; pass < passes && alive; ++pass) {
         const int ntok = min(kTok, s.nt - pass * kTok);
-        // activation rows: one TMA tile when the pass's rows are contiguous (w2
-        // items: h rows; the shared expert's w13 items: x rows), else one bulk
-        // copy per token, issued by lane tl
+        // activation rows: one TMA box per half when the pass's rows are
+        // contiguous (w2 items: h rows; the shared expert's w13 items: x rows),
+        // else one bulk copy per token, issued by lane tl
         const bool xt = !it.a || s.e < 0;
         const uint8_t* xsrc = nullptr;
         if (!xt && lane < ntok) xsrc = p.xq + (size_t)token_of(p, tb, s, pass * kTok + lane) * p.H;
@@ -396,6 +397,15 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
               }
             }
           }
+          if (lane == 0 && pass == 0 && st == 0 && nxt < total) {
+            // look ahead: load the readiness of the next item's expert now, so
+            // that a w2 item rarely waits on a round trip when it starts
+            const Item nit = decode_item(nxt, nA_sh, nA_r, totA, nB, has_shared);
+            if (!nit.a && !s_rdy[nit.slot]) {
+              pre_slot = nit.slot;
+              pre_val = ld_relaxed(p.ready + nit.slot);
+            }
+          }
           ++gs;
         }
         __syncwarp();
@@ -421,23 +431,111 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
         mbar_wait(full + (j % nst), (j / nst) & 1u, status);
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncwarp();
+  } else if (warp == kEW) {
+    // ================================================================ epilogue
+    // Adds the four k-block partial sums of each finished 32-row group, applies
+    // SwiGLU (w13) or stores the rows (w2), and runs the group counters and the
+    // re-quantisation of h, so the consumer warps never wait on global atomics.
+    uint32_t uses = 0;
+    int cur = -1;
+    Item it{};
+    Slot s{};
+    while (true) {
+      if (!mbar_wait(red_full, uses & 1u, status)) break;
+      const int4 em = *reinterpret_cast<const int4*>(epi);
+      if (em.w) break;  // end
+      const int item = em.x, pass = em.y & 0xffff, qr = em.y >> 16, flags = em.z;
+      if (item != cur) {
+        cur = item;
+        it = decode_item(item, nA_sh, nA_r, totA, nB, has_shared);
+        s = make_slot(p, tb, it.slot, has_shared);
+      }
+      const int ntok = min(kTok, s.nt - pass * kTok);
+      if (it.a) {
+        const int rg = kSliceA * it.idx;
+        for (int idx = lane; idx < kSliceA * ntok; idx += 32) {
+          const int i = idx % kSliceA, tl = idx / kSliceA;
+          float gsum = 0.f, usum = 0.f;
+#pragma unroll
+          for (int w = 0; w < kKH; ++w) {
+            gsum += red[(0 * kKH + w) * 16 * kTok + i * kTok + tl];
+            usum += red[(1 * kKH + w) * 16 * kTok + i * kTok + tl];
+          }
+          const float z = fminf(gsum, p.limit);
+          const float hv = z / (1.f + expf(-z)) * fminf(fmaxf(usum, -p.limit), p.limit);
+          p.h[(size_t)(s.hbase + pass * kTok + tl) * p.Imax + rg + i] = hv;
+        }
+      } else {
+        const int row0 = kRowsB * it.idx + kRowsQ * qr;
+        for (int idx = lane; idx < kRowsQ * ntok; idx += 32) {
+          const int rr = idx % kRowsQ, tl = idx / kRowsQ, n = pass * kTok + tl;
+          float v = 0.f;
+#pragma unroll
+          for (int w = 0; w < kKH; ++w) v += red[((rr >> 4) * kKH + w) * 16 * kTok + (rr & 15) * kTok + tl];
+          float* dst = s.e < 0 ? p.shared_out + (size_t)n * p.H : p.rows + (size_t)tb.sorted[s.o + n] * p.H;
+          dst[row0 + rr] = v;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(red_empty);
+      ++uses;
+      if (it.a && (flags & kPassEnd) && pass * kTok + kTok >= s.nt) {
+        // the 8th finished slice of a 128-column group quantises the group
+        int last = 0;
+        if (lane == 0) {
+          __threadfence();
+          last = atomicAdd(p.gcount + it.slot * p.gI + it.idx / (kBlock / kSliceA), 1) == kBlock / kSliceA - 1;
+        }
+        if (__shfl_sync(0xffffffffu, last, 0)) {
+          __threadfence();
+          const int grp = it.idx / (kBlock / kSliceA);
+          constexpr int kQB = 8;  // rows whose loads are in flight together
+          for (int n0 = 0; n0 < s.nt; n0 += kQB) {
+            float4 v[kQB];
+#pragma unroll
+            for (int j = 0; j < kQB; ++j)
+              if (n0 + j < s.nt)
+                v[j] = __ldcg(reinterpret_cast<const float4*>(p.h + (size_t)(s.hbase + n0 + j) * p.Imax +
+                                                              grp * kBlock + 4 * lane));
+#pragma unroll
+            for (int j = 0; j < kQB; ++j) {
+              if (n0 + j < s.nt) {
+                const size_t row = (size_t)(s.hbase + n0 + j);
+                const float amax =
+                    warp_max(fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
+                const float scl = group_scale(amax, p.e8m0);
+                *reinterpret_cast<uint32_t*>(p.hq + row * p.Imax + grp * kBlock + 4 * lane) =
+                    f32x4_to_e4m3x4(__fdiv_rn(v[j].x, scl), __fdiv_rn(v[j].y, scl), __fdiv_rn(v[j].z, scl),
+                                    __fdiv_rn(v[j].w, scl));
+                if (lane == 0) p.hs[row * p.hsS + grp] = scl;
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) {
+            __threadfence();
+            if (!(fault && it.slot == 0)) atomicAdd(p.ready + it.slot, 1);
+          }
+        }
+      }
+    }
   } else {
     // ================================================================ consumers
-    CBar cb{cbar_mem, 0u, status};
     const int tile = warp / kKH, kw = warp % kKH;  // this warp's 16-row tile; k-blocks kw and kKH + kw
     float acc[TT][4];
 #pragma unroll
     for (int t = 0; t < TT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-    uint32_t gs = 0;
+    uint32_t gs = 0, red_uses = 0;
     int cur = -1;  // item whose description below is current
     Item it{};
     Slot s{};
     int nkbK = 0;
+    bool ok = true;
     while (true) {
       const int si = gs % nst;
-      if (!mbar_wait(full + si, (gs / nst) & 1u, status)) break;
+      if (!mbar_wait(full + si, (gs / nst) & 1u, status)) { ok = false; break; }
       const int4 mt = *reinterpret_cast<const int4*>(meta + 4 * si);
-      const int item = mt.x, pass = mt.y & 0xffff, qr = mt.y >> 16, kb0 = mt.z, flags = mt.w;
+      const int item = mt.x, pass = mt.y & 0xffff, kb0 = mt.z, flags = mt.w;
       if (flags & kEnd) break;
       if (flags & kSkip) {
         __syncwarp();
@@ -476,28 +574,30 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
           const float ws = scs[tile];  // A: gate / up block scale; B: the same scale twice
 #pragma unroll
           for (int t = 0; t < TT; ++t) {
-            const int tok = t * 8 + g;
-            uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
-            if (tok < ntok) {
-              if (xt) {  // TMA box [token][kb 4][128 B], 128-byte swizzle, one per half
-                const uint32_t xh = xb + h * C::kXHalf;
-                x0 = lds128(swz(xh, tok * kKH + kw, q));
-                x1 = lds128(swz(xh, tok * kKH + kw, q + 4));
-              } else {   // one bulk row per token, 1088-byte pitch
-                x0 = lds128(xb + tok * kXStride + kl * kBlock + q * 16);
-                x1 = lds128(xb + tok * kXStride + kl * kBlock + q * 16 + 64);
+            if (t * 8 < ntok) {  // token tiles past the pass do no work
+              const int tok = t * 8 + g;
+              uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
+              if (tok < ntok) {
+                if (xt) {  // TMA box [token][kb 4][128 B], 128-byte swizzle, one per half
+                  const uint32_t xh = xb + h * C::kXHalf;
+                  x0 = lds128(swz(xh, tok * kKH + kw, q));
+                  x1 = lds128(swz(xh, tok * kKH + kw, q + 4));
+                } else {   // one bulk row per token, 1088-byte pitch
+                  x0 = lds128(xb + tok * kXStride + kl * kBlock + q * 16);
+                  x1 = lds128(xb + tok * kXStride + kl * kBlock + q * 16 + 64);
+                }
               }
+              float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+              mma_span_e4m3(c0, a0[0], a1[0], x0);
+              mma_span_e4m3(c1, a0[1], a1[1], x1);
+              // scales of tokens past the pass are not fetched: keep those columns at zero
+              const float f0 = t * 8 + 2 * q < ntok ? ws * scs[2 + t * 8 + 2 * q] : 0.f;
+              const float f1 = t * 8 + 2 * q + 1 < ntok ? ws * scs[2 + t * 8 + 2 * q + 1] : 0.f;
+              acc[t][0] += (c0[0] + c1[0]) * f0;
+              acc[t][1] += (c0[1] + c1[1]) * f1;
+              acc[t][2] += (c0[2] + c1[2]) * f0;
+              acc[t][3] += (c0[3] + c1[3]) * f1;
             }
-            float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-            mma_span_e4m3(c0, a0[0], a1[0], x0);
-            mma_span_e4m3(c1, a0[1], a1[1], x1);
-            // scales of tokens past the pass are not fetched: keep those columns at zero
-            const float f0 = t * 8 + 2 * q < ntok ? ws * scs[2 + t * 8 + 2 * q] : 0.f;
-            const float f1 = t * 8 + 2 * q + 1 < ntok ? ws * scs[2 + t * 8 + 2 * q + 1] : 0.f;
-            acc[t][0] += (c0[0] + c1[0]) * f0;
-            acc[t][1] += (c0[1] + c1[1]) * f1;
-            acc[t][2] += (c0[2] + c1[2]) * f0;
-            acc[t][3] += (c0[3] + c1[3]) * f1;
           }
         }
       }
@@ -506,86 +606,31 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
       ++gs;
 
       if (flags & kLast) {
-        // ---- epilogue of a 32-row group: add the four k-block partial sums
+        // ---- hand this 32-row group's partial sums to the epilogue warp
+        if (!mbar_wait(red_empty, (red_uses & 1u) ^ 1u, status)) { ok = false; break; }
         float* r = red + (tile * kKH + kw) * 16 * kTok;
 #pragma unroll
         for (int t = 0; t < TT; ++t) {
-          const int tl = t * 8 + 2 * q;
-          r[g * kTok + tl] = acc[t][0];
-          r[g * kTok + tl + 1] = acc[t][1];
-          r[(g + 8) * kTok + tl] = acc[t][2];
-          r[(g + 8) * kTok + tl + 1] = acc[t][3];
+          if (t * 8 < ntok) {
+            const int tl = t * 8 + 2 * q;
+            r[g * kTok + tl] = acc[t][0];
+            r[g * kTok + tl + 1] = acc[t][1];
+            r[(g + 8) * kTok + tl] = acc[t][2];
+            r[(g + 8) * kTok + tl + 1] = acc[t][3];
+          }
           acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
         }
-        if (!cb.sync()) break;
-        if (it.a) {
-          const int rg = kSliceA * it.idx;
-          for (int idx = tid; idx < kSliceA * ntok; idx += kCW * 32) {
-            const int i = idx % kSliceA, tl = idx / kSliceA;
-            float gsum = 0.f, usum = 0.f;
-#pragma unroll
-            for (int w = 0; w < kKH; ++w) {
-              gsum += red[(0 * kKH + w) * 16 * kTok + i * kTok + tl];
-              usum += red[(1 * kKH + w) * 16 * kTok + i * kTok + tl];
-            }
-            const float z = fminf(gsum, p.limit);
-            const float hv = z / (1.f + expf(-z)) * fminf(fmaxf(usum, -p.limit), p.limit);
-            p.h[(size_t)(s.hbase + pass * kTok + tl) * p.Imax + rg + i] = hv;
-          }
-        } else {
-          const int row0 = kRowsB * it.idx + kRowsQ * qr;
-          for (int idx = tid; idx < kRowsQ * ntok; idx += kCW * 32) {
-            const int rr = idx % kRowsQ, tl = idx / kRowsQ, n = pass * kTok + tl;
-            float v = 0.f;
-#pragma unroll
-            for (int w = 0; w < kKH; ++w) v += red[((rr >> 4) * kKH + w) * 16 * kTok + (rr & 15) * kTok + tl];
-            float* dst = s.e < 0 ? p.shared_out + (size_t)n * p.H : p.rows + (size_t)tb.sorted[s.o + n] * p.H;
-            dst[row0 + rr] = v;
-          }
-        }
-        if (!cb.sync()) break;
-        if (it.a && (flags & kPassEnd) && pass * kTok + kTok >= s.nt && warp == 0) {
-          // warp 0 alone: the 8th finished slice of a 128-column group
-          // quantises the group; the other warps go on with the stream
-          int last = 0;
-          if (lane == 0) {
-            __threadfence();
-            last = atomicAdd(p.gcount + it.slot * p.gI + it.idx / (kBlock / kSliceA), 1) ==
-                   kBlock / kSliceA - 1;
-          }
-          if (__shfl_sync(0xffffffffu, last, 0)) {
-            __threadfence();
-            const int grp = it.idx / (kBlock / kSliceA);
-            constexpr int kQB = 8;  // rows whose loads are in flight together
-            for (int n0 = 0; n0 < s.nt; n0 += kQB) {
-              float4 v[kQB];
-#pragma unroll
-              for (int j = 0; j < kQB; ++j)
-                if (n0 + j < s.nt)
-                  v[j] = __ldcg(reinterpret_cast<const float4*>(p.h + (size_t)(s.hbase + n0 + j) * p.Imax +
-                                                                grp * kBlock + 4 * lane));
-#pragma unroll
-              for (int j = 0; j < kQB; ++j) {
-                if (n0 + j < s.nt) {
-                  const size_t row = (size_t)(s.hbase + n0 + j);
-                  const float amax =
-                      warp_max(fmaxf(fmaxf(fabsf(v[j].x), fabsf(v[j].y)), fmaxf(fabsf(v[j].z), fabsf(v[j].w))));
-                  const float scl = group_scale(amax, p.e8m0);
-                  *reinterpret_cast<uint32_t*>(p.hq + row * p.Imax + grp * kBlock + 4 * lane) =
-                      f32x4_to_e4m3x4(__fdiv_rn(v[j].x, scl), __fdiv_rn(v[j].y, scl), __fdiv_rn(v[j].z, scl),
-                                      __fdiv_rn(v[j].w, scl));
-                  if (lane == 0) p.hs[row * p.hsS + grp] = scl;
-                }
-              }
-            }
-            __syncwarp();
-            if (lane == 0) {
-              __threadfence();
-              if (!(fault && it.slot == 0)) atomicAdd(p.ready + it.slot, 1);
-            }
-          }
-        }
+        if (warp == 0 && lane == 0) *reinterpret_cast<int4*>(epi) = make_int4(item, mt.y, flags, 0);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(red_full);
+        ++red_uses;
       }
+    }
+    // tell the epilogue warp to finish (after it has taken the last group)
+    if (ok && mbar_wait(red_empty, (red_uses & 1u) ^ 1u, status)) {
+      if (warp == 0 && lane == 0) *reinterpret_cast<int4*>(epi) = make_int4(0, 0, 0, 1);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(red_full);
     }
   }
   __syncthreads();
@@ -634,7 +679,7 @@ bool map_w2(CUtensorMap* m, const uint8_t* base, int H, int I, int n) {
 
 template <int TT>
 size_t other_smem(const ExpertArgs& a, int nst) {
-  return (size_t)nst * (4 * sizeof(int) + 2 * sizeof(uint64_t)) + sizeof(uint64_t) +
+  return (size_t)nst * (4 * sizeof(int) + 2 * sizeof(uint64_t)) + 2 * sizeof(uint64_t) + 4 * sizeof(int) +
          sizeof(float) * ((size_t)2 * kKH * 16 * Cfg<TT>::kTok) +
          sizeof(int) * (3 * a.E + 2 + a.Mk + 4 + Cfg<TT>::kTok) + 1024;
 }
