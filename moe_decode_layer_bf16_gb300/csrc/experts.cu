@@ -74,9 +74,9 @@ struct Cfg {
   static constexpr int kTok = 8 * TT;
   static constexpr int kXBytes = ((kTok * kXStride + 1023) / 1024) * 1024;
   static constexpr int kXHalf = kTok * kKH * 128;  // one activation box (tokens x 4 k-blocks)
-  static constexpr int kSBytes = ((kKBS * (2 + kTok) * 4 + 1023) / 1024) * 1024;  // block scales [kKBS][2 + kTok]
-  static constexpr int kSlot = kWBytes + kXBytes + kSBytes;
-  static constexpr int kNSTMax = 4;
+  static constexpr int kSlot = kWBytes + kXBytes;
+  static constexpr int kRedBufs = TT == 4 ? 1 : 2;  // epilogue hand-off buffers
+  static constexpr int kNSTMax = 5;
 };
 
 // ------------------------------------------------------------- PTX wrappers
@@ -204,14 +204,13 @@ struct TmaMaps {
   CUtensorMap hq;  // h codes [Mk + M][Imax/128][128], same box
 };
 
-MOE_DEV void cp_async4(void* dst, const void* src, bool valid) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(su32(dst)), "l"(src), "r"(valid ? 4 : 0)
-               : "memory");
-}
-// Arrive on `bar` once this thread's earlier cp.async copies have landed (the
-// barrier's expected count includes this arrival).
-MOE_DEV void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(su32(bar)) : "memory");
+// L1-cached load of a block scale.  Weight and x scales are never written in
+// this kernel; an h-scale row is read only after its expert's ready signal and
+// is alone in its 128-byte line, so no stale line can be cached before it.
+MOE_DEV float ld_ca(const float* p) {
+  float v;
+  asm volatile("ld.global.ca.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
 }
 
 MOE_DEV int ld_relaxed(const int* p) {
@@ -225,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
                                                               int nst) {
   using C = Cfg<TT>;
   constexpr int kTok = C::kTok;
-  constexpr int kSV = 2 + kTok;  // scale values per k-block of a stage: 2 weight + kTok activation
+  constexpr int kRedF = 2 * kKH * 16 * kTok;  // floats of one epilogue hand-off buffer
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (su32(smem_raw) & 1023)) & 1023);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
@@ -236,11 +235,11 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
   int* meta = reinterpret_cast<int*>(smem + (size_t)nst * C::kSlot);              // [nst][4]
   uint64_t* full = reinterpret_cast<uint64_t*>(meta + 4 * nst);                    // [nst]
   uint64_t* empty = full + nst;                                                    // [nst]
-  uint64_t* red_full = empty + nst;                                                // [1]
-  uint64_t* red_empty = red_full + 1;                                              // [1]
-  float* red = reinterpret_cast<float*>(red_empty + 1);                            // [2][kKH][16][kTok]
-  int* epi = reinterpret_cast<int*>(red + 2 * kKH * 16 * kTok);                    // [4]
-  int* s_off = epi + 4;                                                            // [E+1]
+  uint64_t* red_full = empty + nst;                                                // [2]
+  uint64_t* red_empty = red_full + 2;                                              // [2]
+  float* red = reinterpret_cast<float*>(red_empty + 2);                            // [bufs][2][kKH][16][kTok]
+  int* epi = reinterpret_cast<int*>(red + C::kRedBufs * kRedF);                    // [2][4]
+  int* s_off = epi + 8;                                                            // [E+1]
   int* s_act = s_off + (p.E + 1);                                                  // [E]
   int* s_sorted = s_act + p.E;                                                     // [Mk]
   int* s_misc = s_sorted + p.Mk;                                                   // [4]
@@ -250,11 +249,13 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
 
   if (tid == 0) {
     for (int i = 0; i < nst; ++i) {
-      mbar_init(full + i, 1 + kKBS);  // producer's expect-tx arrival + one scale-copy arrival per k-block
+      mbar_init(full + i, 1);  // the producer's expect-tx arrival
       mbar_init(empty + i, kCW);
     }
-    mbar_init(red_full, kCW);
-    mbar_init(red_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(red_full + b, kCW);
+      mbar_init(red_empty + b, 1);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_misc[0] = *(volatile int*)(p.hdr + kHdrActive);
   }
@@ -284,6 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
     bool alive = true;
     int item = 0;
     int pre_slot = -1, pre_val = 0;  // lane 0: readiness of the next item's expert, loaded ahead
+    int pre_done = 0;                // lane 0: w13 items finished, loaded ahead
+    bool all_ready = false;          // every w13 item (and every h group) is done
     if (lane == 0) item = atomicAdd(p.hdr + kHdrQueue, 1);
     item = __shfl_sync(0xffffffffu, item, 0);
     while (alive && item < total) {
@@ -296,7 +299,14 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
       const int nq = it.a ? 1 : kRowsB / kRowsQ;    // row quarters (B)
       const int nstage = nkg * nq;
       bool skip = false;
-      if (!it.a && !s_rdy[it.slot]) {
+      if (!it.a && !all_ready && lane == 0 && pre_done >= totA) {
+        // all w13 work is done: one acquire covers every expert from now on
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        all_ready = true;
+      }
+      all_ready = __shfl_sync(0xffffffffu, all_ready, 0);
+      if (!it.a && !all_ready && !s_rdy[it.slot]) {
         // w2 items need the expert's quantised h: all of its groups
         int sk = 0;
         if (lane == 0) {
@@ -321,8 +331,6 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
         __syncwarp();  // the other lanes' scale reads come after lane 0's acquire
         skip = __shfl_sync(0xffffffffu, sk, 0) != 0;
       }
-      const float* w_sc = it.a ? (s.e < 0 ? p.sw13_s : p.w13_s + (size_t)s.e * (2 * p.I / kBlock) * nkbH)
-                               : (s.e < 0 ? p.sw2_s : p.w2_s + (size_t)s.e * nkbH * (p.I / kBlock));
       const int rg = kSliceA * it.idx;
       const int passes = skip ? 1 : (s.nt + kTok - 1) / kTok;
       for (int pass = 0; pass < passes && alive; ++pass) {
@@ -333,12 +341,6 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
         const bool xt = !it.a || s.e < 0;
         const uint8_t* xsrc = nullptr;
         if (!xt && lane < ntok) xsrc = p.xq + (size_t)token_of(p, tb, s, pass * kTok + lane) * p.H;
-        // scale source rows of the pass's tokens (x scales for w13, h scales for w2)
-        for (int tl = lane; tl < kTok; tl += 32)
-          s_srow[tl] = tl >= ntok ? -1 : (it.a ? token_of(p, tb, s, pass * kTok + tl) : s.hbase + pass * kTok + tl);
-        __syncwarp();
-        const float* xs_base = it.a ? p.xs : p.hs;
-        const int xs_stride = it.a ? nkbH : p.hsS;
         for (int st = 0; st < (skip ? 1 : nstage); ++st) {
           const int si = gs % nst;
           int ok = 1;
@@ -349,7 +351,6 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
           const int nkv = min(kKBS, nkbK - kb0);
           uint8_t* wdst = ring + (size_t)si * C::kSlot;
           uint8_t* xdst = wdst + kWBytes;
-          float* sdst = reinterpret_cast<float*>(wdst + kWBytes + C::kXBytes);
           if (lane == 0) {
             const int fl = skip ? kSkip
                                 : ((st == 0 ? kFirst : 0) | (st - qr * nkg == nkg - 1 ? kLast : 0) |
@@ -359,41 +360,28 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
             else mbar_expect_tx(full + si, kWBytes + (xt ? 2 * C::kXHalf : ntok * nkv * kBlock));
           }
           __syncwarp();
-          if (lane < kKBS) {
-            // block scales of k-block kb0 + lane: [w_gate/w, w_up/w, x or h of each token]
-            const int kb = kb0 + lane;
-            if (!skip && kb < nkbK) {
-              float* d = sdst + lane * kSV;
-              const float* w0 = it.a ? w_sc + (size_t)(rg / kBlock) * nkbH + kb : w_sc + (size_t)it.idx * nkbK + kb;
-              const float* w1 = it.a ? w_sc + (size_t)((s.Ie + rg) / kBlock) * nkbH + kb : w0;
-              cp_async4(d, w0, true);
-              cp_async4(d + 1, w1, true);
-              for (int tl = 0; tl < ntok; ++tl) cp_async4(d + 2 + tl, xs_base + (size_t)s_srow[tl] * xs_stride + kb, true);
-            }
-            cp_async_arrive(full + si);
-          }
           if (!skip) {
             if (!xt && lane < ntok)
               bulk_load(xdst + lane * kXStride, xsrc + (size_t)kb0 * kBlock, nkv * kBlock, full + si);
-            if (lane == 0) {
-              // two boxes of 4 k-blocks each: [kb0, kb0 + 4) and [kb0 + 4, kb0 + 8)
-              for (int h = 0; h < 2; ++h) {
-                const int kh = kb0 + h * kKH;
+            // the stage's tensor copies, one per lane in one instruction: lanes 0/1
+            // the two weight boxes [kb0, kb0 + 4) and [kb0 + 4, kb0 + 8), lanes 2/3
+            // the matching activation boxes
+            if (lane < 4) {
+              const int h = lane & 1, kh = kb0 + h * kKH;
+              if (lane < 2) {
                 uint8_t* wd = wdst + h * kWHalf;
-                uint8_t* xd = xdst + h * C::kXHalf;
                 if (it.a) {
-                  if (s.e < 0) {
-                    tma_load_5d(wd, &maps.sw13, 0, kh, rg, 0, 0, full + si);
-                    tma_load_3d(xd, &maps.xq, 0, kh, pass * kTok, full + si);
-                  } else {
-                    tma_load_5d(wd, &maps.w13, 0, kh, rg, 0, s.e, full + si);
-                  }
+                  if (s.e < 0) tma_load_5d(wd, &maps.sw13, 0, kh, rg, 0, 0, full + si);
+                  else tma_load_5d(wd, &maps.w13, 0, kh, rg, 0, s.e, full + si);
                 } else {
                   const int r0 = kRowsB * it.idx + kRowsQ * qr;
                   if (s.e < 0) tma_load_4d(wd, &maps.sw2, 0, kh, r0, 0, full + si);
                   else tma_load_4d(wd, &maps.w2, 0, kh, r0, s.e, full + si);
-                  tma_load_3d(xd, &maps.hq, 0, kh, s.hbase + pass * kTok, full + si);
                 }
+              } else if (xt) {
+                uint8_t* xd = xdst + h * C::kXHalf;
+                if (it.a) tma_load_3d(xd, &maps.xq, 0, kh, pass * kTok, full + si);
+                else tma_load_3d(xd, &maps.hq, 0, kh, s.hbase + pass * kTok, full + si);
               }
             }
           }
@@ -401,9 +389,12 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
             // look ahead: load the readiness of the next item's expert now, so
             // that a w2 item rarely waits on a round trip when it starts
             const Item nit = decode_item(nxt, nA_sh, nA_r, totA, nB, has_shared);
-            if (!nit.a && !s_rdy[nit.slot]) {
-              pre_slot = nit.slot;
-              pre_val = ld_relaxed(p.ready + nit.slot);
+            if (!nit.a && !all_ready) {
+              pre_done = ld_relaxed(p.hdr + kHdrDoneA);
+              if (!s_rdy[nit.slot]) {
+                pre_slot = nit.slot;
+                pre_val = ld_relaxed(p.ready + nit.slot);
+              }
             }
           }
           ++gs;
@@ -422,14 +413,12 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
           meta[4 * si + 3] = kEnd;
           mbar_arrive(full + si);
         }
-        if (lane < kKBS) cp_async_arrive(full + si);
         ++gs;
       }
     }
     if (lane == 0)
       for (uint32_t j = (gs > (uint32_t)nst ? gs - nst : 0); j < gs; ++j)
         mbar_wait(full + (j % nst), (j / nst) & 1u, status);
-    asm volatile("cp.async.wait_all;" ::: "memory");
     __syncwarp();
   } else if (warp == kEW) {
     // ================================================================ epilogue
@@ -441,9 +430,11 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
     Item it{};
     Slot s{};
     while (true) {
-      if (!mbar_wait(red_full, uses & 1u, status)) break;
-      const int4 em = *reinterpret_cast<const int4*>(epi);
+      const int b = uses % C::kRedBufs, ph = (uses / C::kRedBufs) & 1;
+      if (!mbar_wait(red_full + b, ph, status)) break;
+      const int4 em = *reinterpret_cast<const int4*>(epi + 4 * b);
       if (em.w) break;  // end
+      const float* rb = red + b * kRedF;
       const int item = em.x, pass = em.y & 0xffff, qr = em.y >> 16, flags = em.z;
       if (item != cur) {
         cur = item;
@@ -458,8 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
           float gsum = 0.f, usum = 0.f;
 #pragma unroll
           for (int w = 0; w < kKH; ++w) {
-            gsum += red[(0 * kKH + w) * 16 * kTok + i * kTok + tl];
-            usum += red[(1 * kKH + w) * 16 * kTok + i * kTok + tl];
+            gsum += rb[(0 * kKH + w) * 16 * kTok + i * kTok + tl];
+            usum += rb[(1 * kKH + w) * 16 * kTok + i * kTok + tl];
           }
           const float z = fminf(gsum, p.limit);
           const float hv = z / (1.f + expf(-z)) * fminf(fmaxf(usum, -p.limit), p.limit);
@@ -471,13 +462,13 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
           const int rr = idx % kRowsQ, tl = idx / kRowsQ, n = pass * kTok + tl;
           float v = 0.f;
 #pragma unroll
-          for (int w = 0; w < kKH; ++w) v += red[((rr >> 4) * kKH + w) * 16 * kTok + (rr & 15) * kTok + tl];
+          for (int w = 0; w < kKH; ++w) v += rb[((rr >> 4) * kKH + w) * 16 * kTok + (rr & 15) * kTok + tl];
           float* dst = s.e < 0 ? p.shared_out + (size_t)n * p.H : p.rows + (size_t)tb.sorted[s.o + n] * p.H;
           dst[row0 + rr] = v;
         }
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(red_empty);
+      if (lane == 0) mbar_arrive(red_empty + b);
       ++uses;
       if (it.a && (flags & kPassEnd) && pass * kTok + kTok >= s.nt) {
         // the 8th finished slice of a 128-column group quantises the group
@@ -511,12 +502,15 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
               }
             }
           }
+          // the codes are read with TMA (async proxy) by other CTAs
+          asm volatile("fence.proxy.async.global;" ::: "memory");
           __syncwarp();
           if (lane == 0) {
             __threadfence();
             if (!(fault && it.slot == 0)) atomicAdd(p.ready + it.slot, 1);
           }
         }
+        if (lane == 0) atomicAdd(p.hdr + kHdrDoneA, 1);  // released by the fences above
       }
     }
   } else {
@@ -526,10 +520,12 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
 #pragma unroll
     for (int t = 0; t < TT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
     uint32_t gs = 0, red_uses = 0;
-    int cur = -1;  // item whose description below is current
+    int cur = -1, cur_pass = -1;  // item (and pass) whose description below is current
     Item it{};
     Slot s{};
     int nkbK = 0;
+    const float* wsr = nullptr;   // this warp's weight-scale row (16-row tile's 128-row block)
+    const float* xsr[TT][2];      // scale rows of this thread's token columns (or null)
     bool ok = true;
     while (true) {
       const int si = gs % nst;
@@ -545,11 +541,39 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
       }
       if (item != cur) {
         cur = item;
+        cur_pass = -1;
         it = decode_item(item, nA_sh, nA_r, totA, nB, has_shared);
         s = make_slot(p, tb, it.slot, has_shared);
         nkbK = it.a ? nkbH : s.Ie / kBlock;
+        const int rg = kSliceA * it.idx;
+        wsr = it.a ? (s.e < 0 ? p.sw13_s : p.w13_s + (size_t)s.e * (2 * p.I / kBlock) * nkbH) +
+                         (size_t)((tile == 0 ? rg : s.Ie + rg) / kBlock) * nkbH
+                   : (s.e < 0 ? p.sw2_s : p.w2_s + (size_t)s.e * nkbH * (p.I / kBlock)) + (size_t)it.idx * nkbK;
       }
       const int ntok = min(kTok, s.nt - pass * kTok);
+      if (pass != cur_pass) {
+        cur_pass = pass;
+#pragma unroll
+        for (int t = 0; t < TT; ++t)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int tl = t * 8 + 2 * q + j;
+            xsr[t][j] = tl >= ntok ? nullptr
+                                   : (it.a ? p.xs + (size_t)token_of(p, tb, s, pass * kTok + tl) * nkbH
+                                           : p.hs + (size_t)(s.hbase + pass * kTok + tl) * p.hsS);
+          }
+      }
+      // block scales of this warp's two k-blocks: issued first, used after the MMAs
+      float wsc[2], xsc[2][TT][2];
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int kb = kb0 + h * kKH + kw;
+        wsc[h] = kb < nkbK ? ld_ca(wsr + kb) : 0.f;
+#pragma unroll
+        for (int t = 0; t < TT; ++t)
+#pragma unroll
+          for (int j = 0; j < 2; ++j) xsc[h][t][j] = (kb < nkbK && xsr[t][j]) ? ld_ca(xsr[t][j] + kb) : 0.f;
+      }
 
       // ---- this warp's tile of its two k-blocks of the stage (one per box)
 #pragma unroll
@@ -560,8 +584,6 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
           const uint32_t wb = sb + h * kWHalf;
           const uint32_t xb = sb + kWBytes;
           const bool xt = (flags & kXT) != 0;
-          const float* scs = reinterpret_cast<const float*>(ring + (size_t)si * C::kSlot + kWBytes + C::kXBytes) +
-                             kl * kSV;
           // A box [gu 2][row 16][kb 4][128 B] (tile 0 gate, tile 1 up);
           // B box [row 32][kb 4][128 B] (tile 0 rows 0..15, tile 1 rows 16..31):
           // either way row r of tile t is 128-byte row (16 t + r) * 4 + k-block
@@ -571,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
             a0[sp] = lds128(swz(wb, (tile * 16 + g) * kKH + kw, q + 4 * sp));
             a1[sp] = lds128(swz(wb, (tile * 16 + g + 8) * kKH + kw, q + 4 * sp));
           }
-          const float ws = scs[tile];  // A: gate / up block scale; B: the same scale twice
+          const float ws = wsc[h];
 #pragma unroll
           for (int t = 0; t < TT; ++t) {
             if (t * 8 < ntok) {  // token tiles past the pass do no work
@@ -590,9 +612,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
               float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
               mma_span_e4m3(c0, a0[0], a1[0], x0);
               mma_span_e4m3(c1, a0[1], a1[1], x1);
-              // scales of tokens past the pass are not fetched: keep those columns at zero
-              const float f0 = t * 8 + 2 * q < ntok ? ws * scs[2 + t * 8 + 2 * q] : 0.f;
-              const float f1 = t * 8 + 2 * q + 1 < ntok ? ws * scs[2 + t * 8 + 2 * q + 1] : 0.f;
+              // token columns past the pass have scale 0
+              const float f0 = ws * xsc[h][t][0], f1 = ws * xsc[h][t][1];
               acc[t][0] += (c0[0] + c1[0]) * f0;
               acc[t][1] += (c0[1] + c1[1]) * f1;
               acc[t][2] += (c0[2] + c1[2]) * f0;
@@ -607,8 +628,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
 
       if (flags & kLast) {
         // ---- hand this 32-row group's partial sums to the epilogue warp
-        if (!mbar_wait(red_empty, (red_uses & 1u) ^ 1u, status)) { ok = false; break; }
-        float* r = red + (tile * kKH + kw) * 16 * kTok;
+        const int b = red_uses % C::kRedBufs;
+        if (!mbar_wait(red_empty + b, ((red_uses / C::kRedBufs) & 1u) ^ 1u, status)) { ok = false; break; }
+        float* r = red + b * kRedF + (tile * kKH + kw) * 16 * kTok;
 #pragma unroll
         for (int t = 0; t < TT; ++t) {
           if (t * 8 < ntok) {
@@ -620,17 +642,18 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
           }
           acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
         }
-        if (warp == 0 && lane == 0) *reinterpret_cast<int4*>(epi) = make_int4(item, mt.y, flags, 0);
+        if (warp == 0 && lane == 0) *reinterpret_cast<int4*>(epi + 4 * b) = make_int4(item, mt.y, flags, 0);
         __syncwarp();
-        if (lane == 0) mbar_arrive(red_full);
+        if (lane == 0) mbar_arrive(red_full + b);
         ++red_uses;
       }
     }
-    // tell the epilogue warp to finish (after it has taken the last group)
-    if (ok && mbar_wait(red_empty, (red_uses & 1u) ^ 1u, status)) {
-      if (warp == 0 && lane == 0) *reinterpret_cast<int4*>(epi) = make_int4(0, 0, 0, 1);
+    // tell the epilogue warp to finish (in the next hand-off buffer, once free)
+    const int b = red_uses % C::kRedBufs;
+    if (ok && mbar_wait(red_empty + b, ((red_uses / C::kRedBufs) & 1u) ^ 1u, status)) {
+      if (warp == 0 && lane == 0) *reinterpret_cast<int4*>(epi + 4 * b) = make_int4(0, 0, 0, 1);
       __syncwarp();
-      if (lane == 0) mbar_arrive(red_full);
+      if (lane == 0) mbar_arrive(red_full + b);
     }
   }
   __syncthreads();
@@ -680,7 +703,8 @@ bool map_w2(CUtensorMap* m, const uint8_t* base, int H, int I, int n) {
 template <int TT>
 size_t other_smem(const ExpertArgs& a, int nst) {
   return (size_t)nst * (4 * sizeof(int) + 2 * sizeof(uint64_t)) + 2 * sizeof(uint64_t) + 4 * sizeof(int) +
-         sizeof(float) * ((size_t)2 * kKH * 16 * Cfg<TT>::kTok) +
+         sizeof(float) * ((size_t)Cfg<TT>::kRedBufs * 2 * kKH * 16 * Cfg<TT>::kTok) + 4 * sizeof(int) +
+         2 * sizeof(uint64_t) +
          sizeof(int) * (3 * a.E + 2 + a.Mk + 4 + Cfg<TT>::kTok) + 1024;
 }
 

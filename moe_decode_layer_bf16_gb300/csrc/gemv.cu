@@ -347,6 +347,7 @@ __device__ void router_finish(const RouterDev& r, int M) {
   if (threadIdx.x == 0) {
     r.hdr[kHdrActive] = s_nact;
     r.hdr[kHdrQueue] = 0;
+    r.hdr[kHdrDoneA] = 0;
     r.hdr[kHdrRouterTicket] = 0;
   }
 }

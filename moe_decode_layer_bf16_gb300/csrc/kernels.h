@@ -15,6 +15,7 @@ enum HdrWord {
   kHdrRouterTicket = 2,  // tiles of router logits reduced so far
   kHdrQueue = 3,         // expert-kernel work queue head
   kHdrActive = 4,        // number of routed experts with at least one route
+  kHdrDoneA = 5,         // w13 items finished (h stored and, when due, its group quantised)
   kHdrWords = 64
 };
 constexpr int kMaxRouterTickets = 1024;
