@@ -11,7 +11,6 @@ namespace moe {
 
 namespace {
 
-constexpr int kGemvCtasPerSm = 4;
 constexpr int kGemvMaxCtas = 2048;
 
 size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -99,9 +98,8 @@ int sm_count_cached(int* out) {
   return MOE_OK;
 }
 
-int gemv_grid(long long cells, int sms) {
-  return (int)std::max<long long>(1, std::min<long long>({cells, (long long)sms * kGemvCtasPerSm,
-                                                         (long long)kGemvMaxCtas}));
+int gemv_grid(long long cells, int sms, int per_sm) {
+  return (int)std::max<long long>(1, std::min<long long>({cells, (long long)sms * per_sm, (long long)kGemvMaxCtas}));
 }
 
 }  // namespace
@@ -158,7 +156,7 @@ static int layer_impl(const moe_layer_dims* dims, const moe_layer_weights* w, in
   const int chunk = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
   const long long cells = (long long)((M + chunk - 1) / chunk) * ((E + 63) / 64) * (H / kBlock);
   // at least 4 k-blocks per CTA: a tile then has at most ~nkb/4 + 1 partial sums to add
-  plan_gemv(plan, M, E, H, gemv_grid((cells + 3) / 4, sms));
+  plan_gemv(plan, M, E, H, gemv_grid((cells + 3) / 4, sms, gemv_blocks_per_sm(chunk, true)));
   if ((long long)plan.n_chunks * plan.n_tiles > kMaxRouterTickets) return MOE_ERR_UNSUPPORTED;
   if (gemv_partials_bytes(plan) > gemv_partials_bound(M, E, H)) return MOE_ERR_UNSUPPORTED;
 
@@ -253,7 +251,7 @@ int splitk_gemm_bf16(const void* A, const void* W, void* C, int c_fp32, int M, i
   GemvPlan plan;
   const int chunk = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
   const long long cells = (long long)((M + chunk - 1) / chunk) * ((N + 63) / 64) * (K / kBlock);
-  plan_gemv(plan, M, N, K, gemv_grid(cells, sms));
+  plan_gemv(plan, M, N, K, gemv_grid(cells, sms, gemv_blocks_per_sm(chunk, false)));
   if (gemv_partials_bytes(plan) > gemv_partials_bound(M, N, K)) return MOE_ERR_UNSUPPORTED;
   SplitKArgs a;
   a.A = A; a.W = W; a.C = C; a.c_fp32 = c_fp32 ? 1 : 0; a.alpha = alpha;

@@ -44,6 +44,12 @@ MOE_DEV int ld_acquire(const int* p) {
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialisation may start while its predecessor is still running; it waits
+// here before touching the predecessor's results.  A no-op otherwise.
+MOE_DEV void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel in the stream be scheduled before this one ends.
+MOE_DEV void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 MOE_DEV unsigned long long globaltimer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

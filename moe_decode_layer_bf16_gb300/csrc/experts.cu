@@ -257,8 +257,11 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
       mbar_init(red_empty + b, 1);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    s_misc[0] = *(volatile int*)(p.hdr + kHdrActive);
   }
+  // everything below reads the router kernel's results
+  grid_dep_wait();
+  grid_dep_launch();
+  if (tid == 0) s_misc[0] = *(volatile int*)(p.hdr + kHdrActive);
   __syncthreads();
   const int n_act = s_misc[0];
   for (int i = tid; i <= p.E; i += kThreads) s_off[i] = p.off[i];
@@ -729,8 +732,8 @@ cudaError_t launch_tt(const ExpertArgs& a, TmaMaps& maps, int num_sms, cudaStrea
   if (smem > (size_t)kSmemMax) return cudaErrorInvalidConfiguration;
   cudaError_t err = cudaFuncSetAttribute(experts_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  experts_kernel<TT><<<num_sms, kThreads, smem, s>>>(a, maps, nst);
-  return cudaGetLastError();
+  PdlLaunch L(dim3(num_sms), dim3(kThreads), smem, s);
+  return cudaLaunchKernelEx(&L.cfg, experts_kernel<TT>, a, maps, nst);
 }
 
 }  // namespace

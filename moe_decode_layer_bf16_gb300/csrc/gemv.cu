@@ -59,30 +59,36 @@ __device__ __forceinline__ void gemv_segment(const Gemv& d, int chunk, int tile,
     bv[t] = n < d.M;
     bp[t] = d.A + (size_t)(bv[t] ? n : 0) * rowb + q * 16;
   }
-  uint4 c0[4], c1[4];
+  // weights and activations of the next k-block are loaded before this one's MMAs
+  uint4 c0[4], c1[4], b[TT][4];
 #pragma unroll
   for (int s = 0; s < 4; ++s) {
     c0[s] = ld_stream(w0 + (size_t)kb0 * 256 + s * 64);
     c1[s] = ld_stream(w1 + (size_t)kb0 * 256 + s * 64);
   }
+#pragma unroll
+  for (int t = 0; t < TT; ++t)
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+      b[t][s] = bv[t] ? __ldg(reinterpret_cast<const uint4*>(bp[t] + (size_t)kb0 * 256 + s * 64))
+                      : make_uint4(0, 0, 0, 0);
 #pragma unroll 1
   for (int kb = kb0; kb < kb1; ++kb) {
     const bool more = kb + 1 < kb1;
-    uint4 n0[4], n1[4];
+    uint4 n0[4], n1[4], nb[TT][4];
     if (more) {
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
         n0[s] = ld_stream(w0 + (size_t)(kb + 1) * 256 + s * 64);
         n1[s] = ld_stream(w1 + (size_t)(kb + 1) * 256 + s * 64);
       }
+#pragma unroll
+      for (int t = 0; t < TT; ++t)
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          nb[t][s] = bv[t] ? __ldg(reinterpret_cast<const uint4*>(bp[t] + (size_t)(kb + 1) * 256 + s * 64))
+                           : make_uint4(0, 0, 0, 0);
     }
-    uint4 b[TT][4];
-#pragma unroll
-    for (int t = 0; t < TT; ++t)
-#pragma unroll
-      for (int s = 0; s < 4; ++s)
-        b[t][s] = bv[t] ? __ldg(reinterpret_cast<const uint4*>(bp[t] + (size_t)kb * 256 + s * 64))
-                        : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int t = 0; t < TT; ++t)
 #pragma unroll
@@ -90,6 +96,10 @@ __device__ __forceinline__ void gemv_segment(const Gemv& d, int chunk, int tile,
     if (more) {
 #pragma unroll
       for (int s = 0; s < 4; ++s) { c0[s] = n0[s]; c1[s] = n1[s]; }
+#pragma unroll
+      for (int t = 0; t < TT; ++t)
+#pragma unroll
+        for (int s = 0; s < 4; ++s) b[t][s] = nb[t][s];
     }
   }
 }
@@ -215,9 +225,9 @@ struct RouterDev {
 // Sigmoid top-k of one token by one warp: lane l holds experts l, l+32, ...
 // Slots come out in descending selection value; an exact tie goes to the
 // lower expert id.  Lane j < k ends with slot j's id and unbiased score.
+template <int kPer>
 __device__ __forceinline__ void warp_topk(const RouterDev& r, const float* logit, int lane, int& my_id,
                                           float& my_s) {
-  constexpr int kPer = kMaxExperts / 32;
   float sel[kPer], sc[kPer];
 #pragma unroll
   for (int i = 0; i < kPer; ++i) {
@@ -278,7 +288,8 @@ __device__ void router_finish(const RouterDev& r, int M) {
     for (int t = c0 + warp; t < min(M, c0 + kTopkChunk); t += kThreads / 32) {
     int id;
     float s;
-    warp_topk(r, s_logit + (t - c0) * E, lane, id, s);
+    if (E <= 256) warp_topk<8>(r, s_logit + (t - c0) * E, lane, id, s);
+    else warp_topk<kMaxExperts / 32>(r, s_logit + (t - c0) * E, lane, id, s);
     const float sum = warp_sum(lane < k ? s : 0.f);
     if (lane < k) {
       const float w = s / sum * r.scaling;
@@ -356,7 +367,24 @@ template <int TT>
 __global__ void __launch_bounds__(kThreads) router_kernel(Gemv d, RouterDev r) {
   __shared__ int s_finish;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // (1) FP8 quantisation of x, per token per 128-column group
+  grid_dep_launch();  // the expert kernel may be scheduled on SMs this grid leaves free
+  // (1) logits; the CTA that completes the last tile finishes the routing
+  if (threadIdx.x == 0) s_finish = 0;
+  __syncthreads();
+  const int n_ct = d.n_chunks * d.n_tiles;
+  auto epi = [&](int n, int row, float v) { r.logits[(size_t)n * r.E + row] = v; };
+  auto on_tile = [&] {
+    if (threadIdx.x == 0) {
+      __threadfence();
+      const int old = atomicAdd(r.hdr + kHdrRouterTicket, 1);
+      if (old == n_ct - 1) s_finish = 1;
+    }
+    __syncthreads();
+  };
+  gemv_streamk<TT>(d, epi, on_tile);
+  if (s_finish) router_finish(r, d.M);
+  // (2) FP8 quantisation of x, per token per 128-column group (read only by
+  // the expert kernel, so it runs off the routing's critical path)
   {
     const int nkbH = r.H / kBlock;
     const int groups = d.M * nkbH;
@@ -373,21 +401,6 @@ __global__ void __launch_bounds__(kThreads) router_kernel(Gemv d, RouterDev r) {
       if (lane == 0) r.xs[(size_t)t * nkbH + kb] = sc;
     }
   }
-  // (2) logits, (3) the CTA that completes the last tile finishes the routing
-  if (threadIdx.x == 0) s_finish = 0;
-  __syncthreads();
-  const int n_ct = d.n_chunks * d.n_tiles;
-  auto epi = [&](int n, int row, float v) { r.logits[(size_t)n * r.E + row] = v; };
-  auto on_tile = [&] {
-    if (threadIdx.x == 0) {
-      __threadfence();
-      const int old = atomicAdd(r.hdr + kHdrRouterTicket, 1);
-      if (old == n_ct - 1) s_finish = 1;
-    }
-    __syncthreads();
-  };
-  gemv_streamk<TT>(d, epi, on_tile);
-  if (s_finish) router_finish(r, d.M);
 }
 
 Gemv make_gemv(const GemvPlan& p, const void* A, const void* W, float* partials, unsigned* tickets) {
@@ -425,6 +438,26 @@ void plan_gemv(GemvPlan& p, int M, int N, int K, int G) {
 
 size_t gemv_partials_bytes(const GemvPlan& p) {
   return (size_t)p.n_chunks * p.n_tiles * p.max_segs * p.chunk_tokens * 64 * sizeof(float);
+}
+
+int gemv_blocks_per_sm(int chunk_tokens, bool router) {
+  static int cache[2][3] = {{0, 0, 0}, {0, 0, 0}};
+  const int i = chunk_tokens == 8 ? 0 : (chunk_tokens == 16 ? 1 : 2);
+  int& c = cache[router ? 1 : 0][i];
+  if (!c) {
+    int n = 0;
+    cudaError_t e;
+    if (router)
+      e = i == 0 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, router_kernel<1>, kThreads, 0)
+        : i == 1 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, router_kernel<2>, kThreads, 0)
+                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, router_kernel<4>, kThreads, 0);
+    else
+      e = i == 0 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, splitk_kernel<1>, kThreads, 0)
+        : i == 1 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, splitk_kernel<2>, kThreads, 0)
+                 : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, splitk_kernel<4>, kThreads, 0);
+    c = (e == cudaSuccess && n > 0) ? n : 1;
+  }
+  return c;
 }
 
 cudaError_t launch_splitk(const GemvPlan& p, const SplitKArgs& a, cudaStream_t s) {

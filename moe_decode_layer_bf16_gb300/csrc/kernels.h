@@ -35,6 +35,8 @@ struct GemvPlan {
   int max_segs;      // most segments that cover one (chunk, tile)
 };
 void plan_gemv(GemvPlan& p, int M, int N, int K, int G);
+// resident CTAs per SM of the split-K (router == false) or router kernel
+int gemv_blocks_per_sm(int chunk_tokens, bool router);
 size_t gemv_partials_bytes(const GemvPlan& p);
 
 struct SplitKArgs {
@@ -103,5 +105,23 @@ struct NormArgs {
 cudaError_t launch_rmsnorm(const NormArgs& a, cudaStream_t s);
 
 int device_sm_count();
+
+// Launch configuration that lets a kernel start while its predecessor in the
+// stream finishes (it waits with griddepcontrol.wait before using its results).
+struct PdlLaunch {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  PdlLaunch(dim3 grid, dim3 block, size_t smem, cudaStream_t s) {
+    cfg = cudaLaunchConfig_t{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+};
 
 }  // namespace moe

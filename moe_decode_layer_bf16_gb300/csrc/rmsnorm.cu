@@ -32,6 +32,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
   __shared__ float s_warp[kThreads / 32];
   __shared__ float s_part;
   cg::cluster_group cluster = cg::this_cluster();
+  grid_dep_wait();  // the rows come from the preceding expert kernel
   const int rank = (int)cluster.block_rank();
   const int t = blockIdx.x / kCluster;
   const int ncol = a.H / kCluster, c0 = rank * ncol;
@@ -106,8 +107,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
 
 cudaError_t launch_rmsnorm(const NormArgs& a, cudaStream_t s) {
   if (a.M == 0) return cudaSuccess;
-  rmsnorm_kernel<<<a.M * kCluster, kThreads, 0, s>>>(a);
-  return cudaGetLastError();
+  PdlLaunch L(dim3(a.M * kCluster), dim3(kThreads), 0, s);
+  return cudaLaunchKernelEx(&L.cfg, rmsnorm_kernel, a);
 }
 
 }  // namespace moe
