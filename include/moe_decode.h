@@ -39,7 +39,9 @@ enum moe_status {
   MOE_ERR_UNSUPPORTED = 2,          /* shape outside the supported range        */
   MOE_ERR_WORKSPACE_TOO_SMALL = 3,  /* ws_bytes below the *_workspace_size     */
   MOE_ERR_CUDA = 4,                 /* a CUDA runtime call or launch failed     */
-  MOE_ERR_DEVICE_TIMEOUT = 5        /* a bounded device-side wait gave up       */
+  MOE_ERR_DEVICE_TIMEOUT = 5,       /* a bounded device-side wait gave up       */
+  MOE_ERR_SCRATCH_LIMIT = 6         /* the problem needs more than the library's
+                                       static scratch (splitk_gemm_bf16_noalloc) */
 };
 
 /*
@@ -168,6 +170,30 @@ int splitk_gemm_workspace_size(int M, int N, int K, size_t *bytes);
  */
 int splitk_gemm_bf16(const void *A, const void *W, void *C, int c_fp32, int M, int N, int K,
                      float alpha, void *ws, size_t ws_bytes, void *stream);
+
+/*
+ * splitk_gemm_bf16 without a caller-provided workspace, for callers that
+ * cannot allocate device memory at the point where they run the projection
+ * (for example a plugin whose enqueue function must not call cudaMalloc, or a
+ * runtime that hands out only a fixed pool it owns).  No counterpart on the
+ * source pages: this is an interface convenience of this library.
+ *
+ * Same arguments and result as splitk_gemm_bf16, minus ws / ws_bytes.  The
+ * partial sums and tile counters live in one static device array of
+ * MOE_NOALLOC_SCRATCH_BYTES (8 MiB) in the library, which every GPU that
+ * loads the library holds until the process exits.  Nothing is allocated or
+ * freed.  The first call on a device looks up that array's device address
+ * (cudaGetSymbolAddress) and caches it; make that first call before any work
+ * whose ordering depends on it.  Every call shares the array: calls that may
+ * overlap on the GPU (different streams, or different host threads without
+ * ordering) race and corrupt each other's results; serialise them on one
+ * stream.  A shape whose split needs more scratch than the limit returns
+ * MOE_ERR_SCRATCH_LIMIT before anything is enqueued.  The tile counters are
+ * cleared (cudaMemsetAsync on the array, no allocation) at every call.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
+int splitk_gemm_bf16_noalloc(const void *A, const void *W, void *C, int c_fp32, int M, int N, int K,
+                             float alpha, void *stream);
 
 /*
  * Layer boundary: optional weighted top-k finalize, residual add, RMSNorm

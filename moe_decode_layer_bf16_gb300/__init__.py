@@ -28,6 +28,7 @@ MOE_ERR_UNSUPPORTED = 2
 MOE_ERR_WORKSPACE_TOO_SMALL = 3
 MOE_ERR_CUDA = 4
 MOE_ERR_DEVICE_TIMEOUT = 5
+MOE_ERR_SCRATCH_LIMIT = 6
 
 # kernels one moe_decode_layer call launches (router, experts, boundary)
 LAUNCHES_PER_LAYER = 3
@@ -72,13 +73,14 @@ def lib() -> ctypes.CDLL:
         L.moe_decode_layer_traced.argtypes = L.moe_decode_layer.argtypes + [ctypes.POINTER(_vp)]
         L.splitk_gemm_workspace_size.argtypes = [_i, _i, _i, ctypes.POINTER(_sz)]
         L.splitk_gemm_bf16.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _f, _vp, _sz, _vp]
+        L.splitk_gemm_bf16_noalloc.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _f, _vp]
         L.rmsnorm_residual.argtypes = [_vp, _vp, _vp, _i, _i, _f, _vp, _vp, _i, _vp, _vp, _vp, _vp]
         L.moe_device_status.argtypes = [_vp, _vp]
         L.moe_debug_set_fault.argtypes = [_vp, _i, _vp]
         L.moe_status_str.argtypes = [_i]
         L.moe_status_str.restype = ctypes.c_char_p
         for n in ("moe_decode_workspace_size", "moe_workspace_init", "moe_decode_layer", "moe_decode_layer_traced",
-                  "splitk_gemm_workspace_size", "splitk_gemm_bf16", "rmsnorm_residual",
+                  "splitk_gemm_workspace_size", "splitk_gemm_bf16", "splitk_gemm_bf16_noalloc", "rmsnorm_residual",
                   "moe_device_status", "moe_debug_set_fault"):
             getattr(L, n).restype = ctypes.c_int
         _lib = L
@@ -179,6 +181,18 @@ def splitk_gemm_bf16(A, W, C, workspace, alpha: float = 1.0, stream=None):
                                 float(alpha), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                 _stream(stream))
     _check(rc, "splitk_gemm_bf16")
+
+
+def splitk_gemm_bf16_noalloc(A, W, C, alpha: float = 1.0, stream=None):
+    """splitk_gemm_bf16 with the library's static scratch instead of a caller
+    workspace, for callers that cannot allocate device memory where they run
+    the projection.  Calls that may overlap on the GPU must not share it."""
+    import torch
+    M, K = A.shape
+    N = W.shape[0]
+    rc = lib().splitk_gemm_bf16_noalloc(_ptr(A), _ptr(W), _ptr(C), 1 if C.dtype == torch.float32 else 0, M, N, K,
+                                        float(alpha), _stream(stream))
+    _check(rc, "splitk_gemm_bf16_noalloc")
 
 
 def rmsnorm_residual(residual, gain, out, residual_out, eps: float, x=None, rows=None, route_w=None,

@@ -310,6 +310,7 @@ const char* moe_status_str(int status) {
     case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_SCRATCH_LIMIT: return "problem exceeds the static scratch of the no-allocation entry point";
     default: return "unknown status";
   }
 }

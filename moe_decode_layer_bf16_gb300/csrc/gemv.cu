@@ -18,6 +18,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "../../include/moe_decode.h"
 
 namespace moe {
 
@@ -487,3 +488,49 @@ cudaError_t launch_router(const GemvPlan& p, const RouterArgs& a, cudaStream_t s
 }
 
 }  // namespace moe
+
+// ------------------------------------------------------------------ no-allocation split-K
+// splitk_gemm_bf16_noalloc keeps its partial sums and tile counters in this
+// file-scope device array instead of a caller workspace.  In host code the
+// array's name is only a host-side stand-in: its device address is looked up
+// once per device with cudaGetSymbolAddress and passed to the kernel.
+namespace {
+constexpr size_t kNoallocTicketBytes = 64 * 1024;  // up to 16384 (chunk, tile) counters
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+}  // namespace
+
+extern "C" int splitk_gemm_bf16_noalloc(const void* A, const void* W, void* C, int c_fp32, int M, int N, int K,
+                                        float alpha, void* stream) {
+  using namespace moe;
+  if (M < 1 || N < 1 || K < 1) return MOE_ERR_INVALID_ARG;
+  if (M > 256 || N % 16 || K % kBlock) return MOE_ERR_UNSUPPORTED;
+  if (!A || !W || !C) return MOE_ERR_INVALID_ARG;
+  if (((uintptr_t)A & 15u) || ((uintptr_t)W & 15u)) return MOE_ERR_INVALID_ARG;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  static uint8_t* base[64] = {nullptr};
+  if (!base[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return MOE_ERR_CUDA;
+    base[dev] = reinterpret_cast<uint8_t*>(ptr);
+  }
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return MOE_ERR_CUDA;
+  const int chunk = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
+  const long long cells = (long long)((M + chunk - 1) / chunk) * ((N + 63) / 64) * (K / kBlock);
+  const int per_sm = gemv_blocks_per_sm(chunk, false);
+  GemvPlan plan;
+  plan_gemv(plan, M, N, K, (int)std::max<long long>(1, std::min<long long>({cells, (long long)sms * per_sm, 2048ll})));
+  const size_t tickets = (size_t)plan.n_chunks * plan.n_tiles * sizeof(unsigned);
+  if (tickets > kNoallocTicketBytes || kNoallocTicketBytes + gemv_partials_bytes(plan) > MOE_NOALLOC_SCRATCH_BYTES)
+    return MOE_ERR_SCRATCH_LIMIT;
+  cudaStream_t s = (cudaStream_t)stream;
+  // the counters must start at zero whatever an earlier call left behind
+  if (cudaMemsetAsync(base[dev], 0, tickets, s) != cudaSuccess) return MOE_ERR_CUDA;
+  SplitKArgs a;
+  a.A = A; a.W = W; a.C = C; a.c_fp32 = c_fp32 ? 1 : 0; a.alpha = alpha;
+  a.tickets = reinterpret_cast<unsigned*>(base[dev]);
+  a.partials = reinterpret_cast<float*>(base[dev] + kNoallocTicketBytes);
+  return launch_splitk(plan, a, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
