@@ -50,10 +50,6 @@ namespace {
 
 constexpr int kKBS = 8;                   // k-blocks per stage (two TMA boxes of 4)
 constexpr int kKH = 4;                    // k-blocks per TMA box
-constexpr int kCW = 8;                    // consumer warps: one per (16-row tile, k-block pair) of a stage
-constexpr int kPW = kCW;                  // producer warp
-constexpr int kEW = kCW + 1;              // epilogue warp
-constexpr int kThreads = (kCW + 2) * 32;
 constexpr int kSliceA = 16;               // intermediates per A item
 constexpr int kRowsB = 128;               // w2 rows per B item (one scale block)
 constexpr int kRowsQ = 32;                // w2 rows per stage (a quarter of a B item)
@@ -76,6 +72,14 @@ struct Cfg {
   static constexpr int kXHalf = kTok * kKH * 128;  // one activation box (tokens x 4 k-blocks)
   static constexpr int kSlot = kWBytes + kXBytes;
   static constexpr int kRedBufs = TT == 4 ? 1 : 2;  // epilogue hand-off buffers
+  // consumer warps: each owns one 16-row tile and kKP of the stage's 8 k-blocks
+  // (16 warps x 1 k-block where the registers allow, else 8 warps x 2)
+  static constexpr int kCW = TT == 1 ? 16 : 8;
+  static constexpr int kKP = 2 * kKBS / kCW;   // k-blocks per consumer warp and stage
+  static constexpr int kKW = kKBS / kKP;       // k-block partial sums per tile
+  static constexpr int kPW = kCW;              // producer warp
+  static constexpr int kEW = kCW + 1;          // epilogue warp
+  static constexpr int kThreads = (kCW + 2) * 32;
   static constexpr int kNSTMax = 5;
 };
 
@@ -220,11 +224,12 @@ MOE_DEV int ld_relaxed(const int* p) {
 }
 
 template <int TT>
-__global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, const __grid_constant__ TmaMaps maps,
+__global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArgs p, const __grid_constant__ TmaMaps maps,
                                                               int nst) {
   using C = Cfg<TT>;
   constexpr int kTok = C::kTok;
-  constexpr int kRedF = 2 * kKH * 16 * kTok;  // floats of one epilogue hand-off buffer
+  constexpr int kCW = C::kCW, kKP = C::kKP, kKW = C::kKW, kPW = C::kPW, kEW = C::kEW, kThreads = C::kThreads;
+  constexpr int kRedF = 2 * kKW * 16 * kTok;  // floats of one epilogue hand-off buffer
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (su32(smem_raw) & 1023)) & 1023);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, q = lane & 3;
@@ -237,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
   uint64_t* empty = full + nst;                                                    // [nst]
   uint64_t* red_full = empty + nst;                                                // [2]
   uint64_t* red_empty = red_full + 2;                                              // [2]
-  float* red = reinterpret_cast<float*>(red_empty + 2);                            // [bufs][2][kKH][16][kTok]
+  float* red = reinterpret_cast<float*>(red_empty + 2);                            // [bufs][2][kKW][16][kTok]
   int* epi = reinterpret_cast<int*>(red + C::kRedBufs * kRedF);                    // [2][4]
   int* s_off = epi + 8;                                                            // [E+1]
   int* s_act = s_off + (p.E + 1);                                                  // [E]
@@ -451,9 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
           const int i = idx % kSliceA, tl = idx / kSliceA;
           float gsum = 0.f, usum = 0.f;
 #pragma unroll
-          for (int w = 0; w < kKH; ++w) {
-            gsum += rb[(0 * kKH + w) * 16 * kTok + i * kTok + tl];
-            usum += rb[(1 * kKH + w) * 16 * kTok + i * kTok + tl];
+          for (int w = 0; w < kKW; ++w) {
+            gsum += rb[(0 * kKW + w) * 16 * kTok + i * kTok + tl];
+            usum += rb[(1 * kKW + w) * 16 * kTok + i * kTok + tl];
           }
           const float z = fminf(gsum, p.limit);
           const float hv = z / (1.f + expf(-z)) * fminf(fmaxf(usum, -p.limit), p.limit);
@@ -465,7 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
           const int rr = idx % kRowsQ, tl = idx / kRowsQ, n = pass * kTok + tl;
           float v = 0.f;
 #pragma unroll
-          for (int w = 0; w < kKH; ++w) v += rb[((rr >> 4) * kKH + w) * 16 * kTok + (rr & 15) * kTok + tl];
+          for (int w = 0; w < kKW; ++w) v += rb[((rr >> 4) * kKW + w) * 16 * kTok + (rr & 15) * kTok + tl];
           float* dst = s.e < 0 ? p.shared_out + (size_t)n * p.H : p.rows + (size_t)tb.sorted[s.o + n] * p.H;
           dst[row0 + rr] = v;
         }
@@ -518,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
     }
   } else {
     // ================================================================ consumers
-    const int tile = warp / kKH, kw = warp % kKH;  // this warp's 16-row tile; k-blocks kw and kKH + kw
+    const int tile = warp / kKW, kw = warp % kKW;  // this warp's 16-row tile; k-blocks kw + j kKW, j < kKP
     float acc[TT][4];
 #pragma unroll
     for (int t = 0; t < TT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
@@ -567,10 +572,10 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
           }
       }
       // block scales of this warp's two k-blocks: issued first, used after the MMAs
-      float wsc[2], xsc[2][TT][2];
+      float wsc[kKP], xsc[kKP][TT][2];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int kb = kb0 + h * kKH + kw;
+      for (int h = 0; h < kKP; ++h) {
+        const int kb = kb0 + h * kKW + kw;
         wsc[h] = kb < nkbK ? ld_ca(wsr + kb) : 0.f;
 #pragma unroll
         for (int t = 0; t < TT; ++t)
@@ -578,13 +583,14 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
           for (int j = 0; j < 2; ++j) xsc[h][t][j] = (kb < nkbK && xsr[t][j]) ? ld_ca(xsr[t][j] + kb) : 0.f;
       }
 
-      // ---- this warp's tile of its two k-blocks of the stage (one per box)
+      // ---- this warp's tile of its k-blocks of the stage
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int kl = h * kKH + kw;  // k-block within the stage
+      for (int h = 0; h < kKP; ++h) {
+        const int kl = h * kKW + kw;         // k-block within the stage
+        const int bx = kl / kKH, kk = kl % kKH;  // which of the two boxes, k-block within it
         if (kb0 + kl < nkbK) {
           const uint32_t sb = su32(ring + (size_t)si * C::kSlot);
-          const uint32_t wb = sb + h * kWHalf;
+          const uint32_t wb = sb + bx * kWHalf;
           const uint32_t xb = sb + kWBytes;
           const bool xt = (flags & kXT) != 0;
           // A box [gu 2][row 16][kb 4][128 B] (tile 0 gate, tile 1 up);
@@ -593,8 +599,8 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
           uint4 a0[2], a1[2];
 #pragma unroll
           for (int sp = 0; sp < 2; ++sp) {
-            a0[sp] = lds128(swz(wb, (tile * 16 + g) * kKH + kw, q + 4 * sp));
-            a1[sp] = lds128(swz(wb, (tile * 16 + g + 8) * kKH + kw, q + 4 * sp));
+            a0[sp] = lds128(swz(wb, (tile * 16 + g) * kKH + kk, q + 4 * sp));
+            a1[sp] = lds128(swz(wb, (tile * 16 + g + 8) * kKH + kk, q + 4 * sp));
           }
           const float ws = wsc[h];
 #pragma unroll
@@ -604,9 +610,9 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
               uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
               if (tok < ntok) {
                 if (xt) {  // TMA box [token][kb 4][128 B], 128-byte swizzle, one per half
-                  const uint32_t xh = xb + h * C::kXHalf;
-                  x0 = lds128(swz(xh, tok * kKH + kw, q));
-                  x1 = lds128(swz(xh, tok * kKH + kw, q + 4));
+                  const uint32_t xh = xb + bx * C::kXHalf;
+                  x0 = lds128(swz(xh, tok * kKH + kk, q));
+                  x1 = lds128(swz(xh, tok * kKH + kk, q + 4));
                 } else {   // one bulk row per token, 1088-byte pitch
                   x0 = lds128(xb + tok * kXStride + kl * kBlock + q * 16);
                   x1 = lds128(xb + tok * kXStride + kl * kBlock + q * 16 + 64);
@@ -633,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1) experts_kernel(ExpertArgs p, cons
         // ---- hand this 32-row group's partial sums to the epilogue warp
         const int b = red_uses % C::kRedBufs;
         if (!mbar_wait(red_empty + b, ((red_uses / C::kRedBufs) & 1u) ^ 1u, status)) { ok = false; break; }
-        float* r = red + b * kRedF + (tile * kKH + kw) * 16 * kTok;
+        float* r = red + b * kRedF + (tile * kKW + kw) * 16 * kTok;
 #pragma unroll
         for (int t = 0; t < TT; ++t) {
           if (t * 8 < ntok) {
@@ -706,7 +712,7 @@ bool map_w2(CUtensorMap* m, const uint8_t* base, int H, int I, int n) {
 template <int TT>
 size_t other_smem(const ExpertArgs& a, int nst) {
   return (size_t)nst * (4 * sizeof(int) + 2 * sizeof(uint64_t)) + 2 * sizeof(uint64_t) + 4 * sizeof(int) +
-         sizeof(float) * ((size_t)Cfg<TT>::kRedBufs * 2 * kKH * 16 * Cfg<TT>::kTok) + 4 * sizeof(int) +
+         sizeof(float) * ((size_t)Cfg<TT>::kRedBufs * 2 * Cfg<TT>::kKW * 16 * Cfg<TT>::kTok) + 4 * sizeof(int) +
          2 * sizeof(uint64_t) +
          sizeof(int) * (3 * a.E + 2 + a.Mk + 4 + Cfg<TT>::kTok) + 1024;
 }
@@ -732,7 +738,7 @@ cudaError_t launch_tt(const ExpertArgs& a, TmaMaps& maps, int num_sms, cudaStrea
   if (smem > (size_t)kSmemMax) return cudaErrorInvalidConfiguration;
   cudaError_t err = cudaFuncSetAttribute(experts_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (err != cudaSuccess) return err;
-  PdlLaunch L(dim3(num_sms), dim3(kThreads), smem, s);
+  PdlLaunch L(dim3(num_sms), dim3(Cfg<TT>::kThreads), smem, s);
   return cudaLaunchKernelEx(&L.cfg, experts_kernel<TT>, a, maps, nst);
 }
 
