@@ -13,22 +13,23 @@
 // The step streams each active expert's FP8 weights exactly once and is
 // HBM-bound at every token count of the workload, so the kernel is built as a
 // weight stream that never drains:
-//   * one CTA per SM: one producer warp, eight consumer warps and one
-//     epilogue warp;
+//   * one CTA per SM: one producer warp, 16 consumer warps (8 when a pass
+//     holds 16 tokens) and one epilogue warp;
 //   * work items, taken by the producer from one atomic queue (all w13 items,
 //     shared expert first, then all w2 items):
 //       A item (expert, 16 intermediates): 16 gate + 16 up rows of w13 over H,
 //       B item (expert, 128 rows of w2, one scale block) over I, streamed as
 //       four 32-row groups;
-//   * a stage is one 16 KB TMA tile of weights (4 k-blocks of 128 columns,
-//     128-byte swizzle) plus, per token of the pass, the matching 512 bytes of
-//     its FP8 activation row (1-D bulk copies), all completing on the stage's
-//     mbarrier; the producer runs up to a whole ring of stages ahead, across
-//     item boundaries, so epilogues overlap the stream;
-//   * each consumer warp takes one 16-row tile of one k-block of every stage
-//     (warp-level FP8 MMA, m16n8k32, fp32 accumulate, block scales applied per
-//     k-block); the four k-block partial sums of a tile are added in shared
-//     memory at the end of each 32-row group.
+//   * a stage is 8 k-blocks (1024 columns): two 16 KB TMA boxes of weights
+//     (128-byte swizzle) plus the pass's FP8 activation columns (TMA boxes of
+//     contiguous rows, or one 1-D bulk copy per gathered token row), all
+//     completing on the stage's mbarrier; the producer runs up to a whole
+//     ring of stages ahead, across item boundaries, so epilogues overlap the
+//     stream;
+//   * each consumer warp takes one 16-row tile of one (or two) of the stage's
+//     k-blocks (warp-level FP8 MMA, m16n8k32, fp32 accumulate, block scales
+//     applied per k-block); the epilogue warp adds the k-block partial sums of
+//     each 32-row group, handed over in shared memory.
 // The A item that completes the 8th slice of a 128-column group quantises that
 // group of h for every route; an expert's B items are issued once all of its
 // groups are quantised.  Every wait is bounded (~0.2 s): on expiry the kernel
@@ -59,10 +60,11 @@ constexpr int kXStride = 1088;            // gathered activation row pitch in a 
 constexpr int kSmemMax = 227 * 1024;
 constexpr unsigned long long kWaitNs = 200ull * 1000ull * 1000ull;
 
-// kFirst: first stage of a pass (scales are loaded); kLast: last stage of a
-// 32-row group (its epilogue runs); kPassEnd: last stage of the pass.
-// kXT: the stage's activation rows came as one TMA tile (swizzled), otherwise
-// as one bulk copy per token (rows at a 576-byte pitch).
+// kFirst: first stage of a pass; kLast: last stage of a 32-row group (its
+// epilogue runs); kPassEnd: last stage of the pass; kSkip: nothing was copied
+// (the item gave up waiting), kEnd: no more work.  kXT: the stage's activation
+// rows came as TMA boxes (swizzled), otherwise as one bulk copy per token
+// (rows at a kXStride-byte pitch).
 enum MetaFlag { kFirst = 1, kLast = 2, kSkip = 4, kEnd = 8, kPassEnd = 16, kXT = 32 };
 
 template <int TT>
@@ -71,7 +73,8 @@ struct Cfg {
   static constexpr int kXBytes = ((kTok * kXStride + 1023) / 1024) * 1024;
   static constexpr int kXHalf = kTok * kKH * 128;  // one activation box (tokens x 4 k-blocks)
   static constexpr int kSlot = kWBytes + kXBytes;
-  static constexpr int kRedBufs = TT == 4 ? 1 : 2;  // epilogue hand-off buffers
+  static_assert(TT == 1 || TT == 2, "passes of 8 or 16 tokens");
+  static constexpr int kRedBufs = 2;  // epilogue hand-off buffers
   // consumer warps: each owns one 16-row tile and kKP of the stage's 8 k-blocks
   // (16 warps x 1 k-block where the registers allow, else 8 warps x 2)
   static constexpr int kCW = TT == 1 ? 16 : 8;
@@ -249,7 +252,6 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
   int* s_sorted = s_act + p.E;                                                     // [Mk]
   int* s_misc = s_sorted + p.Mk;                                                   // [4]
   int* s_rdy = s_misc + 4;                                                         // [E+1]
-  int* s_srow = s_rdy + (p.E + 1);                                                 // [kTok]
   int* status = p.hdr + kHdrStatus;
 
   if (tid == 0) {
@@ -286,10 +288,12 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
 
   if (warp == kPW) {
     // ================================================================ producer
-    // Lane 0 owns the ring and the TMA copies; lanes 0..7 fetch each stage's
-    // block scales (one k-block each) with 4-byte cp.async on the stage barrier;
-    // lane tl copies gathered activation row tl.
-    uint32_t gs = 0;
+    // Lane 0 claims items, owns the ring and arms each stage's barrier; lanes
+    // 0..3 issue the stage's tensor copies, lane tl the bulk copy of gathered
+    // activation row tl.
+    uint32_t gs = 0;         // stages issued
+    int si = 0;              // ring slot of stage gs
+    uint32_t ph = 0;         // parity of slot si's current use
     bool alive = true;
     int item = 0;
     int pre_slot = -1, pre_val = 0;  // lane 0: readiness of the next item's expert, loaded ahead
@@ -349,19 +353,19 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
         const bool xt = !it.a || s.e < 0;
         const uint8_t* xsrc = nullptr;
         if (!xt && lane < ntok) xsrc = p.xq + (size_t)token_of(p, tb, s, pass * kTok + lane) * p.H;
+        const int la_st = min(2, nstage - 1);  // stage that looks ahead at the next item
+        int qr = 0, kb0 = 0;                   // row quarter and first k-block of stage st
         for (int st = 0; st < (skip ? 1 : nstage); ++st) {
-          const int si = gs % nst;
           int ok = 1;
-          if (lane == 0) ok = mbar_wait(empty + si, ((gs / nst) & 1u) ^ 1u, status);
+          if (lane == 0) ok = mbar_wait(empty + si, ph ^ 1u, status);
           __syncwarp();  // the slot is rewritten only after the consumers released it
           if (!__shfl_sync(0xffffffffu, ok, 0)) { alive = false; break; }
-          const int qr = st / nkg, kb0 = (st - qr * nkg) * kKBS;
           const int nkv = min(kKBS, nkbK - kb0);
           uint8_t* wdst = ring + (size_t)si * C::kSlot;
           uint8_t* xdst = wdst + kWBytes;
           if (lane == 0) {
             const int fl = skip ? kSkip
-                                : ((st == 0 ? kFirst : 0) | (st - qr * nkg == nkg - 1 ? kLast : 0) |
+                                : ((st == 0 ? kFirst : 0) | (kb0 + kKBS >= nkbK ? kLast : 0) |
                                    (st == nstage - 1 ? kPassEnd : 0) | (xt ? kXT : 0));
             *reinterpret_cast<int4*>(meta + 4 * si) = make_int4(item, pass | (qr << 16), kb0, fl);
             if (skip) mbar_arrive(full + si);
@@ -393,7 +397,7 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
               }
             }
           }
-          if (lane == 0 && pass == 0 && st == 0 && nxt < total) {
+          if (lane == 0 && pass == 0 && st == la_st && nxt < total) {
             // look ahead: load the readiness of the next item's expert now, so
             // that a w2 item rarely waits on a round trip when it starts
             const Item nit = decode_item(nxt, nA_sh, nA_r, totA, nB, has_shared);
@@ -406,6 +410,9 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
             }
           }
           ++gs;
+          if (++si == nst) { si = 0; ph ^= 1u; }
+          kb0 += kKBS;
+          if (kb0 >= nkbK) { kb0 = 0; ++qr; }
         }
         __syncwarp();
       }
@@ -527,7 +534,9 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
     float acc[TT][4];
 #pragma unroll
     for (int t = 0; t < TT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
-    uint32_t gs = 0, red_uses = 0;
+    uint32_t red_uses = 0;
+    int si = 0;       // ring slot of the next stage
+    uint32_t ph = 0;  // its parity
     int cur = -1, cur_pass = -1;  // item (and pass) whose description below is current
     Item it{};
     Slot s{};
@@ -536,15 +545,14 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
     const float* xsr[TT][2];      // scale rows of this thread's token columns (or null)
     bool ok = true;
     while (true) {
-      const int si = gs % nst;
-      if (!mbar_wait(full + si, (gs / nst) & 1u, status)) { ok = false; break; }
+      if (!mbar_wait(full + si, ph, status)) { ok = false; break; }
       const int4 mt = *reinterpret_cast<const int4*>(meta + 4 * si);
       const int item = mt.x, pass = mt.y & 0xffff, kb0 = mt.z, flags = mt.w;
       if (flags & kEnd) break;
       if (flags & kSkip) {
         __syncwarp();
         if (lane == 0) mbar_arrive(empty + si);
-        ++gs;
+        if (++si == nst) { si = 0; ph ^= 1u; }
         continue;
       }
       if (item != cur) {
@@ -633,7 +641,7 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty + si);
-      ++gs;
+      if (++si == nst) { si = 0; ph ^= 1u; }
 
       if (flags & kLast) {
         // ---- hand this 32-row group's partial sums to the epilogue warp
@@ -714,7 +722,7 @@ size_t other_smem(const ExpertArgs& a, int nst) {
   return (size_t)nst * (4 * sizeof(int) + 2 * sizeof(uint64_t)) + 2 * sizeof(uint64_t) + 4 * sizeof(int) +
          sizeof(float) * ((size_t)Cfg<TT>::kRedBufs * 2 * Cfg<TT>::kKW * 16 * Cfg<TT>::kTok) + 4 * sizeof(int) +
          2 * sizeof(uint64_t) +
-         sizeof(int) * (3 * a.E + 2 + a.Mk + 4 + Cfg<TT>::kTok) + 1024;
+         sizeof(int) * (3 * a.E + 2 + a.Mk + 4) + 1024;
 }
 
 // activation codes [rows][K/128][128] bytes; box = 4 k-blocks x `box_rows` rows
@@ -752,9 +760,12 @@ cudaError_t launch_experts(const ExpertArgs& a, int num_sms, cudaStream_t s) {
     return cudaErrorInvalidValue;
   if (a.Is > 0 && (!map_w13(&maps.sw13, a.sw13, a.H, a.Is, 1) || !map_w2(&maps.sw2, a.sw2, a.H, a.Is, 1)))
     return cudaErrorInvalidValue;
-  if (a.M <= 8) return launch_tt<1>(a, maps, num_sms, s);
-  if (a.M <= 16) return launch_tt<2>(a, maps, num_sms, s);
-  return launch_tt<4>(a, maps, num_sms, s);
+  // Passes of 8 tokens: an expert with more tokens (the shared expert above
+  // M = 8) streams its rows once per pass, the repeats from L2.  Wider passes
+  // cost consumer registers and ring stages, and measured slower on the
+  // DeepSeek-V3-shaped layer up to M = 128 tokens; 16-token passes win above.
+  if (a.M <= 128) return launch_tt<1>(a, maps, num_sms, s);
+  return launch_tt<2>(a, maps, num_sms, s);
 }
 
 }  // namespace moe

@@ -76,7 +76,9 @@ def compare(dims, lw, x, res, L=None, tokens=None):
 
 # ------------------------------------------------------------ small layers
 
-@pytest.mark.parametrize("M", [1, 4, 13, 33])
+# 150 tokens: passes of 16 tokens; the others: passes of 8 (33: five passes
+# of the shared expert, the last with one token)
+@pytest.mark.parametrize("M", [1, 4, 13, 33, 150])
 def test_tiny_layer(M):
     lw = synth.make_layer(TINY, seed=0, device=DEV)
     x, res, _ = tie_free_tokens(TINY, lw, M, seed=M, device=DEV)
