@@ -25,6 +25,7 @@ for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
 import argparse
+import hashlib
 import json
 import statistics
 import subprocess
@@ -48,6 +49,11 @@ WORKLOAD = "deepseek-v3-shaped MoE decode layer, H=7168 E=256 k=8 I=Is=2048, M i
 EXPERT_BYTES = 2 * DSV3.inter * DSV3.hidden + DSV3.hidden * DSV3.inter + 4 * (
     (2 * DSV3.inter // 128) * (DSV3.hidden // 128) + (DSV3.hidden // 128) * (DSV3.inter // 128))
 ROUTER_BYTES = DSV3.num_experts * DSV3.hidden * 2
+# DRAM bytes (read + write) per activated expert of one expert-kernel launch, from an
+# ncu capture (profiles/experts_kernel_dsv3_e32_m8.txt) of the kernel built from the
+# experts.cu whose SHA-256 is given; the bench reports no traffic for any other source.
+TRAFFIC_CAPTURE = {"experts_cu_sha256": "a64bc986fd53339d9db27c2ffeb174cf696473f29b94b83e443c048eb103d772",
+                   "bytes_per_expert": (1_277_935_000 + 5_657_088) / 29}
 
 
 def layer_bytes(M: int, unique: int) -> int:
@@ -279,6 +285,11 @@ def run_ours(args, world, rank, local):
 
     peak, peak_kind = load_peaks()
     achieved = exp_bytes_all / (exp_ms_all / 1e3) / 1e9
+    traffic = None
+    src = os.path.join(ROOT, "moe_decode_layer_bf16_gb300", "csrc", "experts.cu")
+    if hashlib.sha256(open(src, "rb").read()).hexdigest() == TRAFFIC_CAPTURE["experts_cu_sha256"]:
+        # per launch, averaged over the launches like `achieved`
+        traffic = round(TRAFFIC_CAPTURE["bytes_per_expert"] * sum(unique[M] + 1 for M in MS) / len(MS))
     for M in MS:
         per_m[str(M)]["frac_of_8TBs"] = round(per_m[str(M)]["layer_gbps"] / 8000.0, 3)
         per_m[str(M)]["frac_of_measured"] = round(per_m[str(M)]["layer_gbps"] / peak, 3)
@@ -323,7 +334,8 @@ def run_ours(args, world, rank, local):
                    "wall_s_timed": round(wall, 4)},
         "roofline": {"bound": "hbm", "kernel": "experts_kernel", "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": f"{peak_kind} HBM copy bandwidth", "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None},
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": round(exp_bytes_all / (len(MS) * args.steps))},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes},
         "gpu_launches": m.LAUNCHES_PER_LAYER * len(MS) * args.steps,
         "timing": "value: events around each plain layer call; per-kernel us and roofline: a second, traced pass",

@@ -64,8 +64,15 @@ constexpr unsigned long long kWaitNs = 200ull * 1000ull * 1000ull;
 // epilogue runs); kPassEnd: last stage of the pass; kSkip: nothing was copied
 // (the item gave up waiting), kEnd: no more work.  kXT: the stage's activation
 // rows came as TMA boxes (swizzled), otherwise as one bulk copy per token
-// (rows at a kXStride-byte pitch).
-enum MetaFlag { kFirst = 1, kLast = 2, kSkip = 4, kEnd = 8, kPassEnd = 16, kXT = 32 };
+// (rows at a kXStride-byte pitch).  kA: a w13 item (x scales), else w2 (h scales).
+enum MetaFlag { kFirst = 1, kLast = 2, kSkip = 4, kEnd = 8, kPassEnd = 16, kXT = 32, kA = 64 };
+
+// Per ring slot, the producer describes the stage to the consumers so that they
+// decode nothing themselves: ints [0, 4) item, pass | quarter << 16, first
+// k-block, flags; [4] tokens of the pass, [5] valid k-blocks of the stage; at
+// the first stage of a pass also [8, 12) the weight-scale rows of the two
+// 16-row tiles (two pointers) and [16, 32) each token's scale-row offset.
+constexpr int kMetaInts = 32;
 
 template <int TT>
 struct Cfg {
@@ -240,8 +247,8 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
 
   // ---- shared memory carve-up: ring slots [W tile | activation rows | scales]
   uint8_t* ring = smem;
-  int* meta = reinterpret_cast<int*>(smem + (size_t)nst * C::kSlot);              // [nst][4]
-  uint64_t* full = reinterpret_cast<uint64_t*>(meta + 4 * nst);                    // [nst]
+  int* meta = reinterpret_cast<int*>(smem + (size_t)nst * C::kSlot);              // [nst][kMetaInts]
+  uint64_t* full = reinterpret_cast<uint64_t*>(meta + kMetaInts * nst);            // [nst]
   uint64_t* empty = full + nst;                                                    // [nst]
   uint64_t* red_full = empty + nst;                                                // [2]
   uint64_t* red_empty = red_full + 2;                                              // [2]
@@ -344,9 +351,23 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
         skip = __shfl_sync(0xffffffffu, sk, 0) != 0;
       }
       const int rg = kSliceA * it.idx;
+      // weight-scale rows of the item's two 16-row tiles (w13: gate, up; w2: one block)
+      const float* wsr0;
+      const float* wsr1;
+      if (it.a) {
+        const float* base = s.e < 0 ? p.sw13_s : p.w13_s + (size_t)s.e * (2 * p.I / kBlock) * nkbH;
+        wsr0 = base + (size_t)(rg / kBlock) * nkbH;
+        wsr1 = base + (size_t)((s.Ie + rg) / kBlock) * nkbH;
+      } else {
+        wsr0 = wsr1 = (s.e < 0 ? p.sw2_s : p.w2_s + (size_t)s.e * nkbH * (p.I / kBlock)) + (size_t)it.idx * nkbK;
+      }
       const int passes = skip ? 1 : (s.nt + kTok - 1) / kTok;
       for (int pass = 0; pass < passes && alive; ++pass) {
         const int ntok = min(kTok, s.nt - pass * kTok);
+        // scale-row offset of this lane's token of the pass (x scales: w13, h scales: w2)
+        int tok_off = 0;
+        if (lane < ntok)
+          tok_off = it.a ? token_of(p, tb, s, pass * kTok + lane) * nkbH : (s.hbase + pass * kTok + lane) * p.hsS;
         // activation rows: one TMA box per half when the pass's rows are
         // contiguous (w2 items: h rows; the shared expert's w13 items: x rows),
         // else one bulk copy per token, issued by lane tl
@@ -363,11 +384,22 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
           const int nkv = min(kKBS, nkbK - kb0);
           uint8_t* wdst = ring + (size_t)si * C::kSlot;
           uint8_t* xdst = wdst + kWBytes;
+          int* md = meta + kMetaInts * si;
+          if (st == 0 && !skip) {
+            // the pass's scale rows, before the slot is armed
+            if (lane < ntok) md[16 + lane] = tok_off;
+            if (lane == 0) {
+              *reinterpret_cast<const float**>(md + 8) = wsr0;
+              *reinterpret_cast<const float**>(md + 10) = wsr1;
+            }
+            __syncwarp();
+          }
           if (lane == 0) {
             const int fl = skip ? kSkip
                                 : ((st == 0 ? kFirst : 0) | (kb0 + kKBS >= nkbK ? kLast : 0) |
-                                   (st == nstage - 1 ? kPassEnd : 0) | (xt ? kXT : 0));
-            *reinterpret_cast<int4*>(meta + 4 * si) = make_int4(item, pass | (qr << 16), kb0, fl);
+                                   (st == nstage - 1 ? kPassEnd : 0) | (xt ? kXT : 0) | (it.a ? kA : 0));
+            *reinterpret_cast<int4*>(md) = make_int4(item, pass | (qr << 16), kb0, fl);
+            *reinterpret_cast<int2*>(md + 4) = make_int2(ntok, nkv);
             if (skip) mbar_arrive(full + si);
             else mbar_expect_tx(full + si, kWBytes + (xt ? 2 * C::kXHalf : ntok * nkv * kBlock));
           }
@@ -425,7 +457,7 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
       if (lane == 0) ok = mbar_wait(empty + si, ((gs / nst) & 1u) ^ 1u, status);
       if (__shfl_sync(0xffffffffu, ok, 0)) {
         if (lane == 0) {
-          meta[4 * si + 3] = kEnd;
+          meta[kMetaInts * si + 3] = kEnd;
           mbar_arrive(full + si);
         }
         ++gs;
@@ -531,23 +563,43 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
   } else {
     // ================================================================ consumers
     const int tile = warp / kKW, kw = warp % kKW;  // this warp's 16-row tile; k-blocks kw + j kKW, j < kKP
+    // this thread's fragment offsets within a slot (A box [gu 2][row 16][kb 4][128 B]
+    // for w13 tiles, B box [row 32][kb 4][128 B] for w2: either way row r of tile t
+    // is 128-byte row (16 t + r) * 4 + k-block of its box; activation boxes
+    // [token][kb 4][128 B]; bulk activation rows at a kXStride pitch)
+    uint32_t a_off[kKP][2][2], xt_off[kKP][TT][2], xb_off[kKP][TT][2];
+#pragma unroll
+    for (int h = 0; h < kKP; ++h) {
+      const int kl = h * kKW + kw, bx = kl / kKH, kk = kl % kKH;
+#pragma unroll
+      for (int sp = 0; sp < 2; ++sp) {
+        a_off[h][sp][0] = bx * kWHalf + swz(0, (tile * 16 + g) * kKH + kk, q + 4 * sp);
+        a_off[h][sp][1] = bx * kWHalf + swz(0, (tile * 16 + g + 8) * kKH + kk, q + 4 * sp);
+      }
+#pragma unroll
+      for (int t = 0; t < TT; ++t) {
+        const int tok = t * 8 + g;
+        xt_off[h][t][0] = kWBytes + bx * C::kXHalf + swz(0, tok * kKH + kk, q);
+        xt_off[h][t][1] = kWBytes + bx * C::kXHalf + swz(0, tok * kKH + kk, q + 4);
+        xb_off[h][t][0] = kWBytes + tok * kXStride + kl * kBlock + q * 16;
+        xb_off[h][t][1] = xb_off[h][t][0] + 64;
+      }
+    }
+    const uint32_t ring_s = su32(ring);
     float acc[TT][4];
 #pragma unroll
     for (int t = 0; t < TT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
     uint32_t red_uses = 0;
     int si = 0;       // ring slot of the next stage
     uint32_t ph = 0;  // its parity
-    int cur = -1, cur_pass = -1;  // item (and pass) whose description below is current
-    Item it{};
-    Slot s{};
-    int nkbK = 0;
     const float* wsr = nullptr;   // this warp's weight-scale row (16-row tile's 128-row block)
     const float* xsr[TT][2];      // scale rows of this thread's token columns (or null)
     bool ok = true;
     while (true) {
       if (!mbar_wait(full + si, ph, status)) { ok = false; break; }
-      const int4 mt = *reinterpret_cast<const int4*>(meta + 4 * si);
-      const int item = mt.x, pass = mt.y & 0xffff, kb0 = mt.z, flags = mt.w;
+      const int* md = meta + kMetaInts * si;
+      const int4 mt = *reinterpret_cast<const int4*>(md);
+      const int item = mt.x, kb0 = mt.z, flags = mt.w;
       if (flags & kEnd) break;
       if (flags & kSkip) {
         __syncwarp();
@@ -555,76 +607,52 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
         if (++si == nst) { si = 0; ph ^= 1u; }
         continue;
       }
-      if (item != cur) {
-        cur = item;
-        cur_pass = -1;
-        it = decode_item(item, nA_sh, nA_r, totA, nB, has_shared);
-        s = make_slot(p, tb, it.slot, has_shared);
-        nkbK = it.a ? nkbH : s.Ie / kBlock;
-        const int rg = kSliceA * it.idx;
-        wsr = it.a ? (s.e < 0 ? p.sw13_s : p.w13_s + (size_t)s.e * (2 * p.I / kBlock) * nkbH) +
-                         (size_t)((tile == 0 ? rg : s.Ie + rg) / kBlock) * nkbH
-                   : (s.e < 0 ? p.sw2_s : p.w2_s + (size_t)s.e * nkbH * (p.I / kBlock)) + (size_t)it.idx * nkbK;
-      }
-      const int ntok = min(kTok, s.nt - pass * kTok);
-      if (pass != cur_pass) {
-        cur_pass = pass;
+      const int2 nn = *reinterpret_cast<const int2*>(md + 4);
+      const int ntok = nn.x, nkv = nn.y;
+      if (flags & kFirst) {
+        // a new pass: its scale rows, as the producer resolved them
+        wsr = *reinterpret_cast<const float* const*>(md + 8 + 2 * tile);
+        const float* xbase = (flags & kA) ? p.xs : p.hs;
 #pragma unroll
         for (int t = 0; t < TT; ++t)
 #pragma unroll
           for (int j = 0; j < 2; ++j) {
             const int tl = t * 8 + 2 * q + j;
-            xsr[t][j] = tl >= ntok ? nullptr
-                                   : (it.a ? p.xs + (size_t)token_of(p, tb, s, pass * kTok + tl) * nkbH
-                                           : p.hs + (size_t)(s.hbase + pass * kTok + tl) * p.hsS);
+            xsr[t][j] = tl < ntok ? xbase + md[16 + tl] : nullptr;
           }
       }
-      // block scales of this warp's two k-blocks: issued first, used after the MMAs
+      // block scales of this warp's k-blocks: issued first, used after the MMAs
       float wsc[kKP], xsc[kKP][TT][2];
 #pragma unroll
       for (int h = 0; h < kKP; ++h) {
-        const int kb = kb0 + h * kKW + kw;
-        wsc[h] = kb < nkbK ? ld_ca(wsr + kb) : 0.f;
+        const int kl = h * kKW + kw, kb = kb0 + kl;
+        wsc[h] = kl < nkv ? ld_ca(wsr + kb) : 0.f;
 #pragma unroll
         for (int t = 0; t < TT; ++t)
 #pragma unroll
-          for (int j = 0; j < 2; ++j) xsc[h][t][j] = (kb < nkbK && xsr[t][j]) ? ld_ca(xsr[t][j] + kb) : 0.f;
+          for (int j = 0; j < 2; ++j) xsc[h][t][j] = (kl < nkv && xsr[t][j]) ? ld_ca(xsr[t][j] + kb) : 0.f;
       }
 
       // ---- this warp's tile of its k-blocks of the stage
+      const uint32_t sb = ring_s + (uint32_t)si * C::kSlot;
+      const bool xt = (flags & kXT) != 0;
 #pragma unroll
       for (int h = 0; h < kKP; ++h) {
-        const int kl = h * kKW + kw;         // k-block within the stage
-        const int bx = kl / kKH, kk = kl % kKH;  // which of the two boxes, k-block within it
-        if (kb0 + kl < nkbK) {
-          const uint32_t sb = su32(ring + (size_t)si * C::kSlot);
-          const uint32_t wb = sb + bx * kWHalf;
-          const uint32_t xb = sb + kWBytes;
-          const bool xt = (flags & kXT) != 0;
-          // A box [gu 2][row 16][kb 4][128 B] (tile 0 gate, tile 1 up);
-          // B box [row 32][kb 4][128 B] (tile 0 rows 0..15, tile 1 rows 16..31):
-          // either way row r of tile t is 128-byte row (16 t + r) * 4 + k-block
+        if (h * kKW + kw < nkv) {
           uint4 a0[2], a1[2];
 #pragma unroll
           for (int sp = 0; sp < 2; ++sp) {
-            a0[sp] = lds128(swz(wb, (tile * 16 + g) * kKH + kk, q + 4 * sp));
-            a1[sp] = lds128(swz(wb, (tile * 16 + g + 8) * kKH + kk, q + 4 * sp));
+            a0[sp] = lds128(sb + a_off[h][sp][0]);
+            a1[sp] = lds128(sb + a_off[h][sp][1]);
           }
           const float ws = wsc[h];
 #pragma unroll
           for (int t = 0; t < TT; ++t) {
             if (t * 8 < ntok) {  // token tiles past the pass do no work
-              const int tok = t * 8 + g;
               uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;
-              if (tok < ntok) {
-                if (xt) {  // TMA box [token][kb 4][128 B], 128-byte swizzle, one per half
-                  const uint32_t xh = xb + bx * C::kXHalf;
-                  x0 = lds128(swz(xh, tok * kKH + kk, q));
-                  x1 = lds128(swz(xh, tok * kKH + kk, q + 4));
-                } else {   // one bulk row per token, 1088-byte pitch
-                  x0 = lds128(xb + tok * kXStride + kl * kBlock + q * 16);
-                  x1 = lds128(xb + tok * kXStride + kl * kBlock + q * 16 + 64);
-                }
+              if (t * 8 + g < ntok) {
+                x0 = lds128(sb + (xt ? xt_off[h][t][0] : xb_off[h][t][0]));
+                x1 = lds128(sb + (xt ? xt_off[h][t][1] : xb_off[h][t][1]));
               }
               float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
               mma_span_e4m3(c0, a0[0], a1[0], x0);
@@ -719,7 +747,7 @@ bool map_w2(CUtensorMap* m, const uint8_t* base, int H, int I, int n) {
 
 template <int TT>
 size_t other_smem(const ExpertArgs& a, int nst) {
-  return (size_t)nst * (4 * sizeof(int) + 2 * sizeof(uint64_t)) + 2 * sizeof(uint64_t) + 4 * sizeof(int) +
+  return (size_t)nst * (kMetaInts * sizeof(int) + 2 * sizeof(uint64_t)) + 2 * sizeof(uint64_t) + 4 * sizeof(int) +
          sizeof(float) * ((size_t)Cfg<TT>::kRedBufs * 2 * Cfg<TT>::kKW * 16 * Cfg<TT>::kTok) + 4 * sizeof(int) +
          2 * sizeof(uint64_t) +
          sizeof(int) * (3 * a.E + 2 + a.Mk + 4) + 1024;
