@@ -109,7 +109,8 @@ int moe_decode_workspace_size(const moe_layer_dims *dims, int max_tokens, size_t
 
 /* Zero a workspace (moe_decode_layer's or splitk_gemm_bf16's) once before its
  * first use.  Calls leave their counters at zero for the next call, so this
- * is needed only once per buffer. */
+ * is needed only once per buffer, and again after a call returned an error
+ * (a launch that failed part-way can leave a counter set). */
 int moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
 
 /*

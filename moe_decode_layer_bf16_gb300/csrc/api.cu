@@ -199,6 +199,7 @@ static int layer_impl(const moe_layer_dims* dims, const moe_layer_weights* w, in
   ea.hs = reinterpret_cast<float*>(ws + L.hs);
   ea.rows = reinterpret_cast<float*>(ws + L.rows);
   ea.shared_out = reinterpret_cast<float*>(ws + L.shared);
+  ea.router_ctas = plan.G;
   if (launch_experts(ea, sms, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (!mark(2)) return MOE_ERR_CUDA;
 

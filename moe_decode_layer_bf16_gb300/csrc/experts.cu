@@ -284,16 +284,13 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  // everything below reads the router kernel's results
-  grid_dep_wait();
+  // The router kernel may still be running: the shared expert's w13 items need
+  // only its first phase (x codes, counters reset), signalled by kHdrXReady;
+  // the producer waits for the whole router grid (griddepcontrol.wait) before
+  // its first routed item and then copies the routing tables to shared memory.
   grid_dep_launch();
-  if (tid == 0) s_misc[0] = *(volatile int*)(p.hdr + kHdrActive);
-  __syncthreads();
-  const int n_act = s_misc[0];
-  for (int i = tid; i <= p.E; i += kThreads) s_off[i] = p.off[i];
-  for (int i = tid; i < n_act; i += kThreads) s_act[i] = p.act[i];
-  for (int i = tid; i < p.Mk; i += kThreads) s_sorted[i] = p.sorted[i];
   for (int i = tid; i <= p.E; i += kThreads) s_rdy[i] = 0;
+  if (tid == 0) s_misc[0] = 0;  // routed experts: 0 until the routing is loaded
   __syncthreads();
   const Tables tb{s_off, s_act, s_sorted};
 
@@ -301,8 +298,6 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
   const int nA_sh = has_shared ? p.Is / kSliceA : 0;
   const int nA_r = p.I / kSliceA;
   const int nB = p.H / kRowsB;
-  const int totA = nA_sh + n_act * nA_r;
-  const int total = totA + ((has_shared ? 1 : 0) + n_act) * nB;
   const int fault = *(volatile int*)(p.hdr + kHdrFault);
 
   if (warp == kPW) {
@@ -318,9 +313,42 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
     int pre_slot = -1, pre_val = 0;  // lane 0: readiness of the next item's expert, loaded ahead
     int pre_done = 0;                // lane 0: w13 items finished, loaded ahead
     bool all_ready = false;          // every w13 item (and every h group) is done
-    if (lane == 0) item = atomicAdd(p.hdr + kHdrQueue, 1);
+    // until the routing is loaded only the shared expert's w13 items are known
+    bool routed = false;
+    int totA = nA_sh, total = nA_sh;
+    if (lane == 0) {
+      // x codes and the reset counters of the router's first phase
+      const unsigned long long t0 = globaltimer_ns();
+      for (long n = 0;; ++n) {
+        if (ld_acquire(p.hdr + kHdrXReady) >= p.router_ctas) break;
+        if (*(volatile int*)status != 0 || n > (1l << 24)) { alive = false; break; }
+        if (globaltimer_ns() - t0 > kWaitNs) {
+          atomicExch(status, MOE_ERR_DEVICE_TIMEOUT);
+          alive = false;
+          break;
+        }
+        __nanosleep(64);
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // x codes are read with TMA
+      if (alive) item = atomicAdd(p.hdr + kHdrQueue, 1);
+    }
+    alive = __shfl_sync(0xffffffffu, alive, 0);
     item = __shfl_sync(0xffffffffu, item, 0);
-    while (alive && item < total) {
+    while (alive) {
+      if (item >= nA_sh && !routed) {
+        // the routing: the router grid has completed and its writes are visible
+        grid_dep_wait();
+        const int n_act = *(volatile int*)(p.hdr + kHdrActive);
+        for (int i = lane; i <= p.E; i += 32) s_off[i] = p.off[i];
+        for (int i = lane; i < n_act; i += 32) s_act[i] = p.act[i];
+        for (int i = lane; i < p.Mk; i += 32) s_sorted[i] = p.sorted[i];
+        if (lane == 0) s_misc[0] = n_act;  // for the epilogue warp's decoding
+        __syncwarp();
+        totA = nA_sh + n_act * nA_r;
+        total = totA + ((has_shared ? 1 : 0) + n_act) * nB;
+        routed = true;
+      }
+      if (item >= total) break;
       int nxt = 0;
       if (lane == 0) nxt = atomicAdd(p.hdr + kHdrQueue, 1);
       const Item it = decode_item(item, nA_sh, nA_r, totA, nB, has_shared);
@@ -497,6 +525,8 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
       const int item = em.x, pass = em.y & 0xffff, qr = em.y >> 16, flags = em.z;
       if (item != cur) {
         cur = item;
+        // routed items come after the producer loaded the routing (and s_misc[0])
+        const int totA = nA_sh + *(volatile int*)s_misc * nA_r;
         it = decode_item(item, nA_sh, nA_r, totA, nB, has_shared);
         s = make_slot(p, tb, it.slot, has_shared);
       }
@@ -715,6 +745,15 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
     }
   }
   __syncthreads();
+  if (tid == 0) {
+    // the last CTA to finish clears the router's x-ready count for the next call
+    // (every CTA has passed its wait on it; the next router starts after this grid)
+    __threadfence();
+    if (atomicAdd(p.hdr + kHdrExit, 1) == (int)gridDim.x - 1) {
+      p.hdr[kHdrXReady] = 0;
+      p.hdr[kHdrExit] = 0;
+    }
+  }
 }
 
 // ------------------------------------------------------------- host side

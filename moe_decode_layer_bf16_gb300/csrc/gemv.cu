@@ -353,14 +353,9 @@ __device__ void router_finish(const RouterDev& r, int M) {
     }
   }
   __syncthreads();
-  // reset the expert kernel's counters and this kernel's ticket
-  for (int i = threadIdx.x; i < r.n_gcount; i += kThreads) r.gcount[i] = 0;
-  for (int i = threadIdx.x; i < r.n_ready; i += kThreads) r.ready[i] = 0;
   if (threadIdx.x == 0) {
     r.hdr[kHdrActive] = s_nact;
-    r.hdr[kHdrQueue] = 0;
-    r.hdr[kHdrDoneA] = 0;
-    r.hdr[kHdrRouterTicket] = 0;
+    r.hdr[kHdrRouterTicket] = 0;  // this kernel's ticket, for the next call
   }
 }
 
@@ -369,7 +364,39 @@ __global__ void __launch_bounds__(kThreads) router_kernel(Gemv d, RouterDev r) {
   __shared__ int s_finish;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   grid_dep_launch();  // the expert kernel may be scheduled on SMs this grid leaves free
-  // (1) logits; the CTA that completes the last tile finishes the routing
+  // (1) FP8 quantisation of x, per token per 128-column group, and (CTA 0) the
+  // reset of the expert kernel's counters: the expert kernel starts on the
+  // shared expert, which needs nothing else, as soon as every CTA has done this
+  {
+    if (blockIdx.x == 0) {
+      for (int i = threadIdx.x; i < r.n_gcount; i += kThreads) r.gcount[i] = 0;
+      for (int i = threadIdx.x; i < r.n_ready; i += kThreads) r.ready[i] = 0;
+      if (threadIdx.x == 0) {
+        r.hdr[kHdrQueue] = 0;
+        r.hdr[kHdrDoneA] = 0;
+      }
+    }
+    const int nkbH = r.H / kBlock;
+    const int groups = d.M * nkbH;
+    const uint8_t* x = d.A;
+    for (int gi = blockIdx.x * (kThreads / 32) + warp; gi < groups; gi += gridDim.x * (kThreads / 32)) {
+      const int t = gi / nkbH, kb = gi % nkbH;
+      const size_t o = (size_t)t * r.H + (size_t)kb * kBlock + 4 * lane;
+      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(x + o * 2));
+      const float v0 = bf16_lo(raw.x), v1 = bf16_hi(raw.x), v2 = bf16_lo(raw.y), v3 = bf16_hi(raw.y);
+      const float amax = warp_max(fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3))));
+      const float sc = group_scale(amax, r.e8m0);
+      *reinterpret_cast<uint32_t*>(r.xq + o) =
+          f32x4_to_e4m3x4(__fdiv_rn(v0, sc), __fdiv_rn(v1, sc), __fdiv_rn(v2, sc), __fdiv_rn(v3, sc));
+      if (lane == 0) r.xs[(size_t)t * nkbH + kb] = sc;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      atomicAdd(r.hdr + kHdrXReady, 1);
+    }
+  }
+  // (2) logits; the CTA that completes the last tile finishes the routing
   if (threadIdx.x == 0) s_finish = 0;
   __syncthreads();
   const int n_ct = d.n_chunks * d.n_tiles;
@@ -384,24 +411,6 @@ __global__ void __launch_bounds__(kThreads) router_kernel(Gemv d, RouterDev r) {
   };
   gemv_streamk<TT>(d, epi, on_tile);
   if (s_finish) router_finish(r, d.M);
-  // (2) FP8 quantisation of x, per token per 128-column group (read only by
-  // the expert kernel, so it runs off the routing's critical path)
-  {
-    const int nkbH = r.H / kBlock;
-    const int groups = d.M * nkbH;
-    const uint8_t* x = d.A;
-    for (int gi = blockIdx.x * 4 + warp; gi < groups; gi += gridDim.x * 4) {
-      const int t = gi / nkbH, kb = gi % nkbH;
-      const size_t o = (size_t)t * r.H + (size_t)kb * kBlock + 4 * lane;
-      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(x + o * 2));
-      const float v0 = bf16_lo(raw.x), v1 = bf16_hi(raw.x), v2 = bf16_lo(raw.y), v3 = bf16_hi(raw.y);
-      const float amax = warp_max(fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3))));
-      const float sc = group_scale(amax, r.e8m0);
-      *reinterpret_cast<uint32_t*>(r.xq + o) =
-          f32x4_to_e4m3x4(__fdiv_rn(v0, sc), __fdiv_rn(v1, sc), __fdiv_rn(v2, sc), __fdiv_rn(v3, sc));
-      if (lane == 0) r.xs[(size_t)t * nkbH + kb] = sc;
-    }
-  }
 }
 
 Gemv make_gemv(const GemvPlan& p, const void* A, const void* W, float* partials, unsigned* tickets) {

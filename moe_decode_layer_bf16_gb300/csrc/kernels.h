@@ -16,6 +16,9 @@ enum HdrWord {
   kHdrQueue = 3,         // expert-kernel work queue head
   kHdrActive = 4,        // number of routed experts with at least one route
   kHdrDoneA = 5,         // w13 items finished (h stored and, when due, its group quantised)
+  kHdrXReady = 6,        // router CTAs that have quantised their share of x (and, CTA 0, reset
+                         // the expert kernel's counters); the expert kernel's last CTA clears it
+  kHdrExit = 7,          // expert-kernel CTAs finished
   kHdrWords = 64
 };
 constexpr int kMaxRouterTickets = 1024;
@@ -92,6 +95,7 @@ struct ExpertArgs {
   int* hdr; int* gcount; int* ready;
   float* h; uint8_t* hq; float* hs;
   float* rows; float* shared_out;
+  int router_ctas;  // CTAs of the router launch that precedes this kernel
 };
 cudaError_t launch_experts(const ExpertArgs& a, int num_sms, cudaStream_t s);
 
