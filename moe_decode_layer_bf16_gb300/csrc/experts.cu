@@ -239,11 +239,6 @@ MOE_DEV float ld_ca(const float* p) {
   return v;
 }
 
-MOE_DEV int ld_relaxed(const int* p) {
-  int v;
-  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 
 template <int TT>
 __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArgs p, const __grid_constant__ TmaMaps maps,
@@ -358,13 +353,17 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
       const int nq = it.a ? 1 : kRowsB / kRowsQ;    // row quarters (B)
       const int nstage = nkg * nq;
       bool skip = false;
-      if (!it.a && !all_ready && lane == 0 && pre_done >= totA) {
-        // all w13 work is done: one acquire covers every expert from now on
-        asm volatile("fence.acq_rel.gpu;" ::: "memory");
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-        all_ready = true;
+      // (lane 0 loads the counts below with ld.acquire, so that its later
+      // reads, and the lanes' copies after the warp barrier, see what the
+      // counted epilogues published; a generic-to-async proxy fence then
+      // orders the TMA reads of h after them)
+      if (!it.a && !all_ready) {
+        // all w13 work done (lane 0's acquire of the count): covers every expert from now on
+        if (__shfl_sync(0xffffffffu, lane == 0 && pre_done >= totA ? 1 : 0, 0)) {
+          all_ready = true;
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+        }
       }
-      all_ready = __shfl_sync(0xffffffffu, all_ready, 0);
       if (!it.a && !all_ready && !s_rdy[it.slot]) {
         // w2 items need the expert's quantised h: all of its groups
         int sk = 0;
@@ -372,7 +371,7 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
           if (!(pre_slot == it.slot && pre_val >= nkbK)) {
             const unsigned long long t0 = globaltimer_ns();
             for (long n = 0;; ++n) {
-              if (ld_relaxed(p.ready + it.slot) >= nkbK) break;
+              if (ld_acquire(p.ready + it.slot) >= nkbK) break;
               if (*(volatile int*)status != 0 || n > (1l << 24)) { sk = 1; break; }
               if (globaltimer_ns() - t0 > kWaitNs) {
                 atomicExch(status, MOE_ERR_DEVICE_TIMEOUT);
@@ -382,12 +381,10 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
               __nanosleep(64);
             }
           }
-          // acquire the expert's h codes and scales, for this thread's TMA reads too
-          asm volatile("fence.acq_rel.gpu;" ::: "memory");
-          asm volatile("fence.proxy.async.global;" ::: "memory");
           if (!sk) s_rdy[it.slot] = 1;
         }
-        __syncwarp();  // the other lanes' scale reads come after lane 0's acquire
+        __syncwarp();  // the lanes' copies and scale reads come after lane 0's acquire
+        asm volatile("fence.proxy.async.global;" ::: "memory");
         skip = __shfl_sync(0xffffffffu, sk, 0) != 0;
       }
       const int rg = kSliceA * it.idx;
@@ -408,12 +405,15 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
         int tok_off = 0;
         if (lane < ntok)
           tok_off = it.a ? token_of(p, tb, s, pass * kTok + lane) * nkbH : (s.hbase + pass * kTok + lane) * p.hsS;
-        // activation rows: one TMA box per half when the pass's rows are
-        // contiguous (w2 items: h rows; the shared expert's w13 items: x rows),
-        // else one bulk copy per token, issued by lane tl
-        const bool xt = !it.a || s.e < 0;
+        // activation rows: the shared expert's w13 items take the pass's x rows
+        // as one TMA box per half; every other item one bulk copy per token
+        // (lane tl: gathered x rows, or the expert's h rows), which at a few
+        // tokens per expert moves only the rows that exist
+        const bool xt = it.a && s.e < 0;
         const uint8_t* xsrc = nullptr;
-        if (!xt && lane < ntok) xsrc = p.xq + (size_t)token_of(p, tb, s, pass * kTok + lane) * p.H;
+        if (!xt && lane < ntok)
+          xsrc = it.a ? p.xq + (size_t)token_of(p, tb, s, pass * kTok + lane) * p.H
+                      : p.hq + (size_t)(s.hbase + pass * kTok + lane) * p.Imax;
         const int la_st = min(2, nstage - 1);  // stage that looks ahead at the next item
         int qr = 0, kb0 = 0;                   // row quarter and first k-block of stage st
         for (int st = 0; st < (skip ? 1 : nstage); ++st) {
@@ -474,10 +474,10 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
             // that a w2 item rarely waits on a round trip when it starts
             const Item nit = decode_item(nxt, nA_sh, nA_r, totA, nB, has_shared);
             if (!nit.a && !all_ready) {
-              pre_done = ld_relaxed(p.hdr + kHdrDoneA);
+              pre_done = ld_acquire(p.hdr + kHdrDoneA);
               if (!s_rdy[nit.slot]) {
                 pre_slot = nit.slot;
-                pre_val = ld_relaxed(p.ready + nit.slot);
+                pre_val = ld_acquire(p.ready + nit.slot);
               }
             }
           }

@@ -223,9 +223,18 @@ struct RouterDev {
   int32_t* user_off;
 };
 
+// Maps a float (not NaN) onto an unsigned key with the same order.
+__device__ __forceinline__ unsigned order_key(float v) {
+  const unsigned u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // Sigmoid top-k of one token by one warp: lane l holds experts l, l+32, ...
 // Slots come out in descending selection value; an exact tie goes to the
-// lower expert id.  Lane j < k ends with slot j's id and unbiased score.
+// lower expert id.  Each slot is two warp reductions: the largest value key
+// over the lanes' best remaining experts, then the smallest id among the
+// lanes that hold it (measured: half the cycles of a shuffle arg-max).
+// Lane j < k ends with slot j's id and unbiased score.
 template <int kPer>
 __device__ __forceinline__ void warp_topk(const RouterDev& r, const float* logit, int lane, int& my_id,
                                           float& my_s) {
@@ -248,24 +257,21 @@ __device__ __forceinline__ void warp_topk(const RouterDev& r, const float* logit
   my_id = -1;
   my_s = 0.f;
   for (int j = 0; j < r.k; ++j) {
+    // this lane's best remaining expert (the lower index wins a tie)
+    int bi = -1;
     float bv = -INFINITY, bs = 0.f;
-    int bi = 0x7fffffff;
 #pragma unroll
     for (int i = 0; i < kPer; ++i) {
-      const int e = lane + 32 * i;
-      if (e < r.E && !((taken >> i) & 1u) && (sel[i] > bv || (sel[i] == bv && e < bi))) {
-        bv = sel[i]; bi = e; bs = sc[i];
+      if (lane + 32 * i < r.E && !((taken >> i) & 1u) && (bi < 0 || sel[i] > bv)) {
+        bv = sel[i]; bs = sc[i]; bi = i;
       }
     }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      const float os = __shfl_xor_sync(0xffffffffu, bs, o);
-      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; bs = os; }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (lane == j) { my_id = bi; my_s = bs; }
+    const unsigned key = bi < 0 ? 0u : order_key(bv);
+    const unsigned kmax = __reduce_max_sync(0xffffffffu, key);
+    const int win = __reduce_min_sync(0xffffffffu, bi >= 0 && key == kmax ? lane + 32 * bi : 0x7fffffff);
+    const float ws = __shfl_sync(0xffffffffu, bs, win & 31);
+    if ((win & 31) == lane) taken |= 1u << (win >> 5);
+    if (lane == j) { my_id = win; my_s = ws; }
   }
 }
 
