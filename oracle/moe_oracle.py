@@ -33,7 +33,9 @@ subsets; routing weights against their sum invariants; route order against a
 brute-force stable sort; RMSNorm against unit RMS; the expert MLP against an
 exact int64 matmul (unit scales, integer activations), against a plain
 SwiGLU library routine with the limit at infinity, and against a dense average
-MLP when k = E with equal scores; the split-K GEMM against a float64 matmul.
+MLP when k = E with equal scores; the split-K GEMM against a float64 matmul;
+the MTP front's concatenation order and normalisation through projections
+that select one half (unit RMS of the selected half, the gathered row).
 The full layer on real shapes is pinned only through these pieces.
 """
 
@@ -391,6 +393,26 @@ def projection(a_bf16, w_bf16, alpha=1.0, out_fp32=False):
     if out_fp32:
         return y.astype(np.float32).astype(np.float64)
     return bf16_round(y)
+
+
+def rmsnorm(x_bf16, gain_bf16, eps):
+    """bf16(x * 1/sqrt(mean(x^2) + eps) * gain), per row; x already bf16 values."""
+    x = np.asarray(x_bf16, np.float64)
+    ms = (x * x).mean(axis=1, keepdims=True)
+    return bf16_round(x / np.sqrt(ms + eps) * np.asarray(gain_bf16, np.float64)[None, :])
+
+
+def mtp_front(ids, embed_bf16, hidden_bf16, enorm_bf16, hnorm_bf16, eps, eh_w_bf16):
+    """The MTP layer's input projection ([draft page] SpecializedDraft.run:
+    the embedding of the input tokens and the previous hidden state, each
+    RMS-normalised with its own gain (enorm / hnorm, one eps), concatenated and
+    projected by eh_proj).  Readings: the embedding half comes first (the name
+    eh_proj: e then h); the concatenated input is bf16, as the BF16 split-K
+    projection reads it.  Returns (A [M, 2H] bf16 values, Y [M, H] bf16)."""
+    ids = np.asarray(ids, np.int64)
+    e = np.asarray(embed_bf16, np.float64)[ids]
+    a = np.concatenate([rmsnorm(e, enorm_bf16, eps), rmsnorm(hidden_bf16, hnorm_bf16, eps)], axis=1)
+    return a, projection(a, eh_w_bf16)
 
 
 def rms(v):

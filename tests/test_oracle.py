@@ -287,3 +287,39 @@ def test_shared_expert_term_present_only_when_given():
     sh = orc.expert_mlp(with_sh["xq"], with_sh["xs"], *L.expert(-1), L.swiglu_limit, L.e8m0)[0]
     assert np.allclose(with_sh["m"] - without["m"], sh, rtol=1e-12, atol=1e-12)
     assert np.abs(sh).max() > 0.1
+
+
+# ------------------------------------------------------------ MTP front
+
+def _cos(a, b):
+    a = np.asarray(a, np.float64).ravel()
+    b = np.asarray(b, np.float64).ravel()
+    return float(a @ b / np.sqrt((a @ a) * (b @ b)))
+
+
+def test_mtp_front_halves_order_gather_and_norm():
+    # projections that select one half of the concatenated input pin the
+    # order (embedding first), the gather and the normalisation by properties:
+    # unit RMS with unit gains, the direction of the selected row, and
+    # invariance to the row's scale
+    rng = np.random.default_rng(5)
+    H, V, M = 256, 16, 3
+    embed = orc.bf16_round(rng.standard_normal((V, H)))
+    hidden = orc.bf16_round(3.0 * rng.standard_normal((M, H)))
+    ones = np.ones(H)
+    ids = np.array([3, 11, 3])
+    eye, zero = np.eye(H), np.zeros((H, H))
+    _, ye = orc.mtp_front(ids, embed, hidden, ones, ones, 1e-6, np.concatenate([eye, zero], axis=1))
+    _, yh = orc.mtp_front(ids, embed, hidden, ones, ones, 1e-6, np.concatenate([zero, eye], axis=1))
+    for t in range(M):
+        assert abs(orc.rms(ye[t]) - 1) < 1e-2 and abs(orc.rms(yh[t]) - 1) < 1e-2
+        assert _cos(ye[t], embed[ids[t]]) > 0.9999
+        assert _cos(yh[t], hidden[t]) > 0.9999
+        assert abs(_cos(ye[t], embed[(ids[t] + 1) % V])) < 0.3  # not a neighbouring row
+    assert np.array_equal(ye[0], ye[2])  # same token id, same row
+    # scale invariance of the normalisation (power-of-two scale: exact in bf16)
+    _, ye4 = orc.mtp_front(ids, 4.0 * embed, hidden, ones, ones, 1e-6, np.concatenate([eye, zero], axis=1))
+    assert np.array_equal(ye, ye4)
+    # gains multiply elementwise after the normalisation: a gain of 2 doubles the half
+    _, ye2 = orc.mtp_front(ids, embed, hidden, 2 * ones, ones, 1e-6, np.concatenate([eye, zero], axis=1))
+    assert np.array_equal(ye2, 2 * ye)
