@@ -54,8 +54,8 @@ ROUTER_BYTES = DSV3.num_experts * DSV3.hidden * 2
 # DRAM bytes (read + write) per activated expert of one expert-kernel launch, from an
 # ncu capture (profiles/experts_kernel_dsv3_e32_m8.txt) of the kernel built from the
 # experts.cu whose SHA-256 is given; the bench reports no traffic for any other source.
-TRAFFIC_CAPTURE = {"experts_cu_sha256": "a64bc986fd53339d9db27c2ffeb174cf696473f29b94b83e443c048eb103d772",
-                   "bytes_per_expert": (1_277_935_000 + 5_657_088) / 29}
+TRAFFIC_CAPTURE = {"experts_cu_sha256": "176c2a05d1b0dfa6287dd389b84f1b3d168837037d60e491e7d17a346e25b0c8",
+                   "bytes_per_expert": (1_278_055_000 + 5_641_216) / 29}
 
 
 def layer_bytes(M: int, unique: int) -> int:
@@ -200,6 +200,84 @@ def run_reference(args, world, rank):
 
 # ------------------------------------------------------------------ GPU arm
 
+def splitk_proj(m, flush_l2, dev, N, K, Ms=(1, 4, 16), reps=5):
+    """The split-K BF16 projection Y[M, N] = A[M, K] W[N, K]^T, L2 flushed
+    before every call: us and GB/s (weights + activations in + out)."""
+    res = {}
+    w = None
+    for M in Ms:
+        a, w_m = synth.make_projection(M, N, K, seed=M, device=dev)
+        w = w_m if w is None else w
+        c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        ws = torch.zeros(m.splitk_gemm_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
+        m.splitk_gemm_bf16(a, w, c, ws)
+        times = []
+        for _ in range(reps):
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            m.splitk_gemm_bf16(a, w, c, ws)
+            e1.record()
+            torch.cuda.synchronize()
+            times.append(e0.elapsed_time(e1))
+        us = 1e3 * statistics.median(times)
+        nbytes = 2 * N * K + 2 * M * K + 2 * M * N
+        res[str(M)] = {"us": round(us, 2), "gbps": round(nbytes / us / 1e3, 1)}
+    del w
+    torch.cuda.empty_cache()
+    return res
+
+
+def graph_chain(m, dims, lw0, MS, n_layers, reps, dev):
+    """A decode chain captured as one CUDA graph: n_layers layers with distinct
+    weights, each layer's out / residual_out feeding the next layer's x /
+    residual, replayed back to back with no L2 flush (each layer's 11 GB of
+    weights evicts the others').  Returns per M: us per layer, tokens/s, GB/s."""
+    layers = [lw0] + [synth.make_layer(dims, seed=10 + i, device=dev) for i in range(n_layers - 1)]
+    res = {}
+    for M in MS:
+        lay = m.MoeDecodeLayer(dims, lw0, max_tokens=M, device=dev)
+        x0, r0 = synth.make_tokens(M, dims.hidden, seed=300 + M, device=dev)
+        bufs = [(torch.empty_like(x0), torch.empty_like(r0)) for _ in range(n_layers)]
+        ids = [torch.empty((M, dims.top_k), dtype=torch.int32, device=dev) for _ in range(n_layers)]
+
+        def run():
+            x, r = x0, r0
+            for i, lw in enumerate(layers):
+                o, ro = bufs[i]
+                m.moe_decode_layer(dims, lw, x, r, o, ro, lay.workspace, topk_ids=ids[i])
+                x, r = o, ro
+
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            run()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            run()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        if lay.status() != m.MOE_OK:
+            raise RuntimeError("device status after graph replay")
+        us = 1e3 * e0.elapsed_time(e1) / (reps * n_layers)
+        nbytes = sum(layer_bytes(M, int(torch.unique(t).numel())) for t in ids) / n_layers
+        res[str(M)] = {"us_per_layer": round(us, 2), "tokens_per_s": round(M * 1e6 / us, 1),
+                       "layer_gbps": round(nbytes / us / 1e3, 1)}
+        del g
+    del layers[1:]
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args, world, rank, local):
     import moe_decode_layer_bf16_gb300 as m
 
@@ -325,6 +403,28 @@ def run_ours(args, world, rank, local):
     e2e_value = sum(MS) * args.steps / (e2e_ms / 1e3)
     io_bytes = sum(2 * M * dims.hidden * 2 for M in MS)
 
+    extra = {}
+    if not args.no_extras:
+        try:
+            extra["graph_chain"] = {
+                "what": "3 layers with distinct weights captured as one CUDA graph, each layer's outputs "
+                        "feeding the next, replayed back to back without L2 flushes",
+                "per_m": graph_chain(m, dims, lw, MS, 3, 10, dev)}
+        except Exception as exc:  # reported, not fatal: the headline does not depend on it
+            extra["graph_chain"] = {"error": f"{type(exc).__name__}: {exc}"}
+        try:
+            extra["splitk_eh_proj"] = {"what": "splitk_gemm_bf16, MTP eh_proj N=7168 K=14336 (205.5 MB), "
+                                               "L2 flushed, median of 5",
+                                       "per_m": splitk_proj(m, flush_l2, dev, 7168, 14336)}
+        except Exception as exc:
+            extra["splitk_eh_proj"] = {"error": f"{type(exc).__name__}: {exc}"}
+        try:
+            extra["splitk_lm_head"] = {"what": "splitk_gemm_bf16, LM head N=129280 K=7168 (1.85 GB), "
+                                               "L2 flushed, median of 5",
+                                       "per_m": splitk_proj(m, flush_l2, dev, 129280, 7168, Ms=(1, 8))}
+        except Exception as exc:
+            extra["splitk_lm_head"] = {"error": f"{type(exc).__name__}: {exc}"}
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         dt, desc = oracle_sample(seed=0)
@@ -350,6 +450,7 @@ def run_ours(args, world, rank, local):
         "timing": "value: events around each plain layer call; per-kernel us and roofline: a second, traced pass",
         "clocks": clk,
         "cpu_baseline": cpu,
+        "extra": extra,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -363,6 +464,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the graph-chain and split-K measurements")
     # profiling aids (smaller resident layer for multi-pass ncu captures)
     ap.add_argument("--num-experts", type=int, default=DSV3.num_experts)
     ap.add_argument("--ms", type=int, nargs="+", default=list(MS))

@@ -212,6 +212,30 @@ int rmsnorm_residual(const void *x, const void *residual, const void *gain, int 
                      float eps, const float *rows, const float *route_w, int k,
                      const float *shared, void *out, void *residual_out, void *stream);
 
+/* The MTP layer's input projection ([draft page] vllm.models.glm5next.nvidia
+ * .specialized_decode.runtime.draft, SpecializedDraft.run: the input tokens'
+ * embeddings and the previous hidden state, each RMS-normalised with its own
+ * gain, concatenated, then eh_proj):
+ *   A[t] = [ bf16(e * rsqrt(mean(e^2) + eps) * enorm) | bf16(h * rsqrt(mean(h^2) + eps) * hnorm) ],
+ *          e = embed[input_ids[t]], h = hidden[t]   (the embedding half first);
+ *   out = A . eh_proj_w^T   (split-K BF16 GEMM, fp32 sums rounded once to bf16).
+ *
+ *   input_ids   int32 [M] device; ids outside [0, vocab) give a zero embedding
+ *               half and MOE_ERR_INVALID_ARG in the workspace status word
+ *               (moe_device_status), never a read outside the table
+ *   embed       bf16 [vocab, H];  hidden bf16 [M, H];  enorm, hnorm bf16 [H]
+ *   eh_proj_w   bf16 [H, 2H] row-major;  out bf16 [M, H]
+ *   workspace   mtp_eh_front_workspace_size(M, H) bytes, zeroed once by
+ *               moe_workspace_init; holds A (readable by the caller after the
+ *               call, at byte offset 256, bf16 [M, 2H]) and the split-K sums
+ * Limits: 1 <= M <= 256, H % 128 == 0, H <= 16384, vocab >= 1; 16-byte aligned
+ * pointers.  Argument errors return before anything is enqueued.  Calls that
+ * share a workspace must be stream-ordered. */
+int mtp_eh_front_workspace_size(int M, int H, size_t *bytes);
+int mtp_eh_front(const int32_t *input_ids, const void *embed, int vocab, const void *hidden,
+                 const void *enorm, const void *hnorm, float eps, const void *eh_proj_w, int M, int H,
+                 void *out, void *ws, size_t ws_bytes, void *stream);
+
 /* Read and clear the device status word of a moe_decode_layer workspace:
  * MOE_OK, or MOE_ERR_DEVICE_TIMEOUT when a bounded wait inside the expert
  * kernel gave up.  Synchronises `stream`; meant for tests and diagnostics. */

@@ -75,13 +75,15 @@ def lib() -> ctypes.CDLL:
         L.splitk_gemm_bf16.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _f, _vp, _sz, _vp]
         L.splitk_gemm_bf16_noalloc.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _f, _vp]
         L.rmsnorm_residual.argtypes = [_vp, _vp, _vp, _i, _i, _f, _vp, _vp, _i, _vp, _vp, _vp, _vp]
+        L.mtp_eh_front_workspace_size.argtypes = [_i, _i, ctypes.POINTER(_sz)]
+        L.mtp_eh_front.argtypes = [_vp, _vp, _i, _vp, _vp, _vp, _f, _vp, _i, _i, _vp, _vp, _sz, _vp]
         L.moe_device_status.argtypes = [_vp, _vp]
         L.moe_debug_set_fault.argtypes = [_vp, _i, _vp]
         L.moe_status_str.argtypes = [_i]
         L.moe_status_str.restype = ctypes.c_char_p
         for n in ("moe_decode_workspace_size", "moe_workspace_init", "moe_decode_layer", "moe_decode_layer_traced",
                   "splitk_gemm_workspace_size", "splitk_gemm_bf16", "splitk_gemm_bf16_noalloc", "rmsnorm_residual",
-                  "moe_device_status", "moe_debug_set_fault"):
+                  "moe_device_status", "moe_debug_set_fault", "mtp_eh_front_workspace_size", "mtp_eh_front"):
             getattr(L, n).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -193,6 +195,23 @@ def splitk_gemm_bf16_noalloc(A, W, C, alpha: float = 1.0, stream=None):
     rc = lib().splitk_gemm_bf16_noalloc(_ptr(A), _ptr(W), _ptr(C), 1 if C.dtype == torch.float32 else 0, M, N, K,
                                         float(alpha), _stream(stream))
     _check(rc, "splitk_gemm_bf16_noalloc")
+
+
+def mtp_eh_front_workspace_size(M: int, H: int) -> int:
+    n = _sz(0)
+    _check(lib().mtp_eh_front_workspace_size(int(M), int(H), ctypes.byref(n)), "mtp_eh_front_workspace_size")
+    return n.value
+
+
+def mtp_eh_front(input_ids, embed, hidden, enorm, hnorm, eps: float, eh_proj_w, out, workspace, stream=None):
+    """out = [enorm(embed[input_ids]) | hnorm(hidden)] . eh_proj_w^T (the MTP
+    layer's input projection); the concatenated input stays in the workspace
+    at byte offset 256 as bf16 [M, 2H]."""
+    M, H = hidden.shape
+    rc = lib().mtp_eh_front(_ptr(input_ids), _ptr(embed), int(embed.shape[0]), _ptr(hidden), _ptr(enorm),
+                            _ptr(hnorm), float(eps), _ptr(eh_proj_w), M, H, _ptr(out), _ptr(workspace),
+                            workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "mtp_eh_front")
 
 
 def rmsnorm_residual(residual, gain, out, residual_out, eps: float, x=None, rows=None, route_w=None,

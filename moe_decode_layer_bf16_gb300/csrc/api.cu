@@ -155,8 +155,10 @@ static int layer_impl(const moe_layer_dims* dims, const moe_layer_weights* w, in
   GemvPlan plan;
   const int chunk = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
   const long long cells = (long long)((M + chunk - 1) / chunk) * ((E + 63) / 64) * (H / kBlock);
-  // at least 4 k-blocks per CTA: a tile then has at most ~nkb/4 + 1 partial sums to add
-  plan_gemv(plan, M, E, H, gemv_grid((cells + 3) / 4, sms, gemv_blocks_per_sm(chunk, true)));
+  // at least 2 (M <= 8) or 4 k-blocks per CTA: shorter runs start the routing
+  // sooner at one token chunk, more partial sums to add cost more above (measured)
+  const int run = M <= 8 ? 2 : 4;
+  plan_gemv(plan, M, E, H, gemv_grid((cells + run - 1) / run, sms, gemv_blocks_per_sm(chunk, true)));
   if ((long long)plan.n_chunks * plan.n_tiles > kMaxRouterTickets) return MOE_ERR_UNSUPPORTED;
   if (gemv_partials_bytes(plan) > gemv_partials_bound(M, E, H)) return MOE_ERR_UNSUPPORTED;
 
@@ -278,6 +280,43 @@ int rmsnorm_residual(const void* x, const void* residual, const void* gain, int 
   na.shared = shared; na.out = out; na.residual_out = residual_out; na.M = M; na.H = H;
   na.k = rows ? k : 0; na.eps = eps;
   return launch_rmsnorm(na, (cudaStream_t)stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// MTP front workspace: a 256-byte header (status word), A = bf16 [M, 2H], then
+// the split-K tickets and partial sums of the eh_proj projection.
+constexpr size_t kMtpHdr = 256;
+
+int mtp_eh_front_workspace_size(int M, int H, size_t* bytes) {
+  if (!bytes || M < 1 || H < 1) return MOE_ERR_INVALID_ARG;
+  if (M > 256 || H % kBlock || H > 16384) return MOE_ERR_UNSUPPORTED;
+  size_t gemm = 0;
+  const int rc = splitk_gemm_workspace_size(M, H, 2 * H, &gemm);
+  if (rc != MOE_OK) return rc;
+  *bytes = kMtpHdr + align_up((size_t)M * 2 * H * 2) + gemm;
+  return MOE_OK;
+}
+
+int mtp_eh_front(const int32_t* input_ids, const void* embed, int vocab, const void* hidden, const void* enorm,
+                 const void* hnorm, float eps, const void* eh_proj_w, int M, int H, void* out, void* ws,
+                 size_t ws_bytes, void* stream) {
+  size_t need = 0;
+  int rc = mtp_eh_front_workspace_size(M, H, &need);
+  if (rc != MOE_OK) return rc;
+  if (vocab < 1 || !(eps >= 0.f)) return MOE_ERR_INVALID_ARG;
+  if (!input_ids || !embed || !hidden || !enorm || !hnorm || !eh_proj_w || !out || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(embed) || !aligned16(hidden) || !aligned16(enorm) || !aligned16(hnorm) || !aligned16(eh_proj_w) ||
+      !aligned16(out) || !aligned16(ws))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* w = reinterpret_cast<uint8_t*>(ws);
+  void* A = w + kMtpHdr;
+  uint8_t* gemm_ws = w + kMtpHdr + align_up((size_t)M * 2 * H * 2);
+  EhNormArgs ea;
+  ea.ids = input_ids; ea.embed = embed; ea.vocab = vocab; ea.hidden = hidden; ea.enorm = enorm; ea.hnorm = hnorm;
+  ea.eps = eps; ea.out = A; ea.M = M; ea.H = H;
+  ea.status = reinterpret_cast<int*>(w) + kHdrStatus;
+  if (launch_eh_norm(ea, (cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
+  return splitk_gemm_bf16(A, eh_proj_w, out, 0, M, H, 2 * H, 1.f, gemm_ws, need - (gemm_ws - w), stream);
 }
 
 int moe_device_status(void* ws, void* stream) {

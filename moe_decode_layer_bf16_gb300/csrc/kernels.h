@@ -108,6 +108,16 @@ struct NormArgs {
 };
 cudaError_t launch_rmsnorm(const NormArgs& a, cudaStream_t s);
 
+struct EhNormArgs {
+  const int32_t* ids; const void* embed; int vocab;
+  const void* hidden; const void* enorm; const void* hnorm;
+  float eps;
+  void* out;  // bf16 [M, 2H]
+  int M, H;
+  int* status;
+};
+cudaError_t launch_eh_norm(const EhNormArgs& a, cudaStream_t s);
+
 int device_sm_count();
 
 // Launch configuration that lets a kernel start while its predecessor in the

@@ -110,6 +110,21 @@ def test_splitk_rejects_before_launch(L):
         m.MOE_ERR_WORKSPACE_TOO_SMALL
 
 
+def test_mtp_front_rejects_before_launch(L):
+    fake = ctypes.c_void_p(0x10000)
+    call = lambda ids, vocab, eps, M, H, ws_bytes: L.mtp_eh_front(ids, fake, vocab, fake, fake, fake, eps, fake, M, H,
+                                                                   fake, fake, ws_bytes, None)
+    assert call(fake, 1000, 1e-6, 4, 7000, 1 << 30) == m.MOE_ERR_UNSUPPORTED   # H % 128
+    assert call(fake, 1000, 1e-6, 300, 7168, 1 << 30) == m.MOE_ERR_UNSUPPORTED  # M > 256
+    assert call(fake, 1000, 1e-6, 0, 7168, 1 << 30) == m.MOE_ERR_INVALID_ARG
+    assert call(None, 1000, 1e-6, 4, 7168, 1 << 30) == m.MOE_ERR_INVALID_ARG
+    assert call(fake, 0, 1e-6, 4, 7168, 1 << 30) == m.MOE_ERR_INVALID_ARG
+    assert call(fake, 1000, -1.0, 4, 7168, 1 << 30) == m.MOE_ERR_INVALID_ARG
+    need = m.mtp_eh_front_workspace_size(4, 7168)
+    assert need >= 256 + 4 * 2 * 7168 * 2 + m.splitk_gemm_workspace_size(4, 7168, 14336)
+    assert call(fake, 1000, 1e-6, 4, 7168, need - 1) == m.MOE_ERR_WORKSPACE_TOO_SMALL
+
+
 def test_rmsnorm_rejects_before_launch(L):
     fake = ctypes.c_void_p(0x10000)
     assert L.rmsnorm_residual(None, fake, fake, 4, 500, 1e-6, None, None, 0, None, fake, fake, None) == \

@@ -200,6 +200,23 @@ def test_splitk_router_form_fp32(M):
     assert orc.max_abs_rel(to_np(c), ref) <= 1e-4
 
 
+@pytest.mark.parametrize("M", [1, 8])
+def test_splitk_lm_head_vocab_width_sampled(M):
+    # the LM-head projection at the DeepSeek-V3 vocabulary width (1.85 GB of
+    # bf16 weights): 1024 sampled output columns, the first and last included
+    N, K = 129280, 7168
+    a, w = synth.make_projection(M, N, K, seed=60 + M, device=DEV)
+    c = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    ws = torch.zeros(m.splitk_gemm_workspace_size(M, N, K), dtype=torch.uint8, device=DEV)
+    m.splitk_gemm_bf16(a, w, c, ws)
+    torch.cuda.synchronize()
+    cols = np.unique(np.concatenate([[0, N - 1], np.random.default_rng(M).choice(N, 1022, replace=False)]))
+    idx = torch.as_tensor(cols, device=DEV)
+    ref = orc.projection(to_np(a), to_np(w.index_select(0, idx)))
+    assert orc.max_abs_rel(to_np(c)[:, cols], ref) <= 1e-2
+    del w
+
+
 # ------------------------------------------------------------ full-size layers
 
 @pytest.fixture(scope="module")
@@ -228,3 +245,74 @@ def test_dsv3_skewed_e8m0_sampled(dsv3_skewed, M):
     dims, lw, L = dsv3_skewed
     x, res, _ = tie_free_tokens(dims, lw, M, seed=2000 + M, zipf=True, device=DEV)
     compare(dims, lw, x, res, L=L, tokens=sorted({0, M - 1}))
+
+
+# ------------------------------------------------------------ MTP front
+
+def _mtp_inputs(M, H, V, seed):
+    gen = torch.Generator(device=DEV).manual_seed(seed)
+    rnd = lambda *s: torch.randn(*s, generator=gen, device=DEV)
+    ids = torch.randint(0, V, (M,), generator=gen, device=DEV, dtype=torch.int32)
+    embed = rnd(V, H).to(torch.bfloat16)
+    hidden = (3 * rnd(M, H)).to(torch.bfloat16)
+    enorm = (1 + 0.1 * rnd(H)).to(torch.bfloat16)
+    hnorm = (1 + 0.1 * rnd(H)).to(torch.bfloat16)
+    return ids, embed, hidden, enorm, hnorm
+
+
+def _run_mtp(ids, embed, hidden, enorm, hnorm, w):
+    M, H = hidden.shape
+    out = torch.empty((M, H), dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(m.mtp_eh_front_workspace_size(M, H), dtype=torch.uint8, device=DEV)
+    m.moe_workspace_init(ws)
+    m.mtp_eh_front(ids, embed, hidden, enorm, hnorm, 1e-6, w, out, ws)
+    torch.cuda.synchronize()
+    assert m.moe_device_status(ws) == m.MOE_OK
+    a = ws[256:256 + M * 2 * H * 2].view(torch.bfloat16).view(M, 2 * H)
+    return to_np(a), to_np(out)
+
+
+@pytest.mark.parametrize("M", [1, 3, 17])
+def test_mtp_front_small(M):
+    H, V = 512, 64
+    ids, embed, hidden, enorm, hnorm = _mtp_inputs(M, H, V, seed=M)
+    w = (0.02 * torch.randn(H, 2 * H, generator=torch.Generator(device=DEV).manual_seed(9), device=DEV)).to(
+        torch.bfloat16)
+    a, out = _run_mtp(ids, embed, hidden, enorm, hnorm, w)
+    ra, ry = orc.mtp_front(to_np(ids), to_np(embed), to_np(hidden), to_np(enorm), to_np(hnorm), 1e-6, to_np(w))
+    # fp32 sums of squares in another order: at most one bf16 ulp off
+    ulp = np.abs(ra) * 2.0 ** -7 + 1e-30
+    assert (np.abs(a - ra) <= ulp).all()
+    assert orc.max_abs_rel(out, ry) <= 1e-2
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_mtp_front_dsv3_sampled(M):
+    # DeepSeek-V3 sizes: H = 7168, vocabulary 129280 (1.85 GB embedding),
+    # eh_proj [7168, 14336]; the input in full, 512 sampled output columns
+    H, V = 7168, 129280
+    ids, embed, hidden, enorm, hnorm = _mtp_inputs(M, H, V, seed=70 + M)
+    _, w = synth.make_projection(1, H, 2 * H, seed=71, device=DEV)
+    a, out = _run_mtp(ids, embed, hidden, enorm, hnorm, w)
+    e = to_np(embed.index_select(0, ids.long()))
+    ra, _ = orc.mtp_front(np.arange(M), e, to_np(hidden), to_np(enorm), to_np(hnorm), 1e-6, np.zeros((1, 2 * H)))
+    ulp = np.abs(ra) * 2.0 ** -7 + 1e-30
+    assert (np.abs(a - ra) <= ulp).mean() > 0.999 and orc.max_abs_rel(a, ra) <= 1e-2
+    cols = np.unique(np.concatenate([[0, H - 1], np.random.default_rng(M).choice(H, 510, replace=False)]))
+    ry = orc.projection(ra, to_np(w.index_select(0, torch.as_tensor(cols, device=DEV))))
+    assert orc.max_abs_rel(out[:, cols], ry) <= 1e-2
+
+
+def test_mtp_front_bad_token_id_is_reported():
+    H, V, M = 512, 64, 2
+    ids, embed, hidden, enorm, hnorm = _mtp_inputs(M, H, V, seed=3)
+    ids[1] = V  # one past the table: a zero embedding half and an error status, no read outside
+    w = torch.zeros(H, 2 * H, dtype=torch.bfloat16, device=DEV)
+    out = torch.empty((M, H), dtype=torch.bfloat16, device=DEV)
+    ws = torch.empty(m.mtp_eh_front_workspace_size(M, H), dtype=torch.uint8, device=DEV)
+    m.moe_workspace_init(ws)
+    m.mtp_eh_front(ids, embed, hidden, enorm, hnorm, 1e-6, w, out, ws)
+    torch.cuda.synchronize()
+    assert m.moe_device_status(ws) == m.MOE_ERR_INVALID_ARG
+    a = to_np(ws[256:256 + M * 2 * H * 2].view(torch.bfloat16).view(M, 2 * H))
+    assert not a[1, :H].any() and a[0, :H].any() and a[1, H:].any()
