@@ -228,6 +228,41 @@ def splitk_proj(m, flush_l2, dev, N, K, Ms=(1, 4, 16), reps=5):
     return res
 
 
+def mtp_front(m, flush_l2, dev, Ms=(1, 4, 16), reps=5):
+    """mtp_eh_front at DeepSeek-V3 sizes (H = 7168, vocabulary 129280,
+    eh_proj [7168, 14336]), L2 flushed before every call."""
+    H, V = 7168, 129280
+    gen = torch.Generator(device=dev).manual_seed(1)
+    embed = torch.randn(V, H, generator=gen, device=dev).to(torch.bfloat16)
+    gains = (1 + 0.1 * torch.randn(2, H, generator=gen, device=dev)).to(torch.bfloat16)
+    _, w = synth.make_projection(1, H, 2 * H, seed=3, device=dev)
+    res = {}
+    for M in Ms:
+        ids = torch.randint(0, V, (M,), generator=gen, device=dev, dtype=torch.int32)
+        hidden = torch.randn(M, H, generator=gen, device=dev).to(torch.bfloat16)
+        out = torch.empty((M, H), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(m.mtp_eh_front_workspace_size(M, H), dtype=torch.uint8, device=dev)
+        m.moe_workspace_init(ws)
+        times = []
+        for r in range(reps + 1):
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            m.mtp_eh_front(ids, embed, hidden, gains[0], gains[1], 1e-6, w, out, ws)
+            e1.record()
+            torch.cuda.synchronize()
+            if r:
+                times.append(e0.elapsed_time(e1))
+        if m.moe_device_status(ws) != m.MOE_OK:
+            raise RuntimeError("mtp_eh_front status")
+        us = 1e3 * statistics.median(times)
+        nbytes = 2 * H * 2 * H + M * (2 * H * 3 + 2 * H * 2 * 2 + 4)  # weights; e, h in, A out + in, out
+        res[str(M)] = {"us": round(us, 2), "gbps": round(nbytes / us / 1e3, 1)}
+    del embed, w
+    torch.cuda.empty_cache()
+    return res
+
+
 def graph_chain(m, dims, lw0, MS, n_layers, reps, dev):
     """A decode chain captured as one CUDA graph: n_layers layers with distinct
     weights, each layer's out / residual_out feeding the next layer's x /
@@ -418,6 +453,12 @@ def run_ours(args, world, rank, local):
                                        "per_m": splitk_proj(m, flush_l2, dev, 7168, 14336)}
         except Exception as exc:
             extra["splitk_eh_proj"] = {"error": f"{type(exc).__name__}: {exc}"}
+        try:
+            extra["mtp_eh_front"] = {"what": "mtp_eh_front, H=7168, vocab 129280, eh_proj [7168, 14336] (205.5 MB), "
+                                             "L2 flushed, median of 5",
+                                     "per_m": mtp_front(m, flush_l2, dev)}
+        except Exception as exc:
+            extra["mtp_eh_front"] = {"error": f"{type(exc).__name__}: {exc}"}
         try:
             extra["splitk_lm_head"] = {"what": "splitk_gemm_bf16, LM head N=129280 K=7168 (1.85 GB), "
                                                "L2 flushed, median of 5",
