@@ -275,40 +275,46 @@ __device__ __forceinline__ void warp_topk(const RouterDev& r, const float* logit
   }
 }
 
-constexpr int kTopkChunk = 8;  // tokens whose logits are staged in shared memory at once
+constexpr int kMaxFinish = 8;  // CTAs that share the routing of the tokens
 
-__device__ void router_finish(const RouterDev& r, int M) {
-  __shared__ int s_ids[kMaxMk];
-  __shared__ int s_cnt[kMaxExperts];
-  __shared__ int s_cur[kMaxExperts];
-  __shared__ __align__(16) float s_logit[kTopkChunk * kMaxExperts];
-  __shared__ int s_nact;
+// Top-k, routing weights and per-token outputs of the tokens of finisher f of
+// F: warp w takes tokens 4 f + w, 4 f + w + 4 F, ...  Each warp stages its
+// token's logits (written by other CTAs: read from L2) in shared memory.
+__device__ void route_tokens(const RouterDev& r, int M, int f, int F) {
+  __shared__ __align__(16) float s_lg[kThreads / 32][kMaxExperts];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int k = r.k, Mk = M * k, E = r.E;
-  __threadfence();
-  for (int c0 = 0; c0 < M; c0 += kTopkChunk) {
-    // one coalesced, batched load of the chunk's logits (written by other CTAs: L2)
-    const int n = min(kTopkChunk, M - c0) * E;
-    for (int i = threadIdx.x * 4; i < n; i += kThreads * 4)
-      *reinterpret_cast<float4*>(s_logit + i) = __ldcg(reinterpret_cast<const float4*>(r.logits + (size_t)c0 * E + i));
-    __syncthreads();
-    for (int t = c0 + warp; t < min(M, c0 + kTopkChunk); t += kThreads / 32) {
+  const int k = r.k, E = r.E;
+  float* lg = s_lg[warp];
+  for (int t = 4 * f + warp; t < M; t += 4 * F) {
+    for (int i = lane * 4; i < E; i += 128)
+      *reinterpret_cast<float4*>(lg + i) = __ldcg(reinterpret_cast<const float4*>(r.logits + (size_t)t * E + i));
+    __syncwarp();
     int id;
     float s;
-    if (E <= 256) warp_topk<8>(r, s_logit + (t - c0) * E, lane, id, s);
-    else warp_topk<kMaxExperts / 32>(r, s_logit + (t - c0) * E, lane, id, s);
+    if (E <= 256) warp_topk<8>(r, lg, lane, id, s);
+    else warp_topk<kMaxExperts / 32>(r, lg, lane, id, s);
     const float sum = warp_sum(lane < k ? s : 0.f);
     if (lane < k) {
       const float w = s / sum * r.scaling;
-      s_ids[t * k + lane] = id;
       r.ids[t * k + lane] = id;
       r.tw[t * k + lane] = w;
       if (r.user_ids) r.user_ids[t * k + lane] = id;
       if (r.user_w) r.user_w[t * k + lane] = w;
     }
-    }
-    __syncthreads();
+    __syncwarp();
   }
+}
+
+// Route order from all tokens' ids (written by the finishers): histogram,
+// exclusive scans, the list of active experts and the stable placement.
+__device__ void route_order(const RouterDev& r, int M) {
+  __shared__ int s_ids[kMaxMk];
+  __shared__ int s_cnt[kMaxExperts];
+  __shared__ int s_cur[kMaxExperts];
+  __shared__ int s_nact;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int k = r.k, Mk = M * k, E = r.E;
+  for (int i = threadIdx.x; i < Mk; i += kThreads) s_ids[i] = __ldcg(r.ids + i);
   for (int e = threadIdx.x; e < E; e += kThreads) s_cnt[e] = 0;
   __syncthreads();
   for (int i = threadIdx.x; i < Mk; i += kThreads) atomicAdd(&s_cnt[s_ids[i]], 1);
@@ -361,7 +367,9 @@ __device__ void router_finish(const RouterDev& r, int M) {
   __syncthreads();
   if (threadIdx.x == 0) {
     r.hdr[kHdrActive] = s_nact;
-    r.hdr[kHdrRouterTicket] = 0;  // this kernel's ticket, for the next call
+    // this kernel's counters, for the next call (every CTA has passed them)
+    r.hdr[kHdrRouterTicket] = 0;
+    r.hdr[kHdrRouterFin] = 0;
   }
 }
 
@@ -402,21 +410,43 @@ __global__ void __launch_bounds__(kThreads) router_kernel(Gemv d, RouterDev r) {
       atomicAdd(r.hdr + kHdrXReady, 1);
     }
   }
-  // (2) logits; the CTA that completes the last tile finishes the routing
-  if (threadIdx.x == 0) s_finish = 0;
-  __syncthreads();
-  const int n_ct = d.n_chunks * d.n_tiles;
+  // (2) logits
   auto epi = [&](int n, int row, float v) { r.logits[(size_t)n * r.E + row] = v; };
-  auto on_tile = [&] {
-    if (threadIdx.x == 0) {
-      __threadfence();
-      const int old = atomicAdd(r.hdr + kHdrRouterTicket, 1);
-      if (old == n_ct - 1) s_finish = 1;
+  gemv_streamk<TT>(d, epi, [] {});
+  // (3) the last F CTAs to finish their logits route the tokens (one warp per
+  // token), once every CTA's logits are in; the last of
+  // them builds the route order.  Every CTA of this grid is resident (it
+  // launches before the expert kernel can), so the wait ends; it is bounded.
+  const int F = min(min(kMaxFinish, (d.M + 3) / 4), (int)gridDim.x);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const int t = atomicAdd(r.hdr + kHdrRouterTicket, 1);
+    s_finish = t >= (int)gridDim.x - F ? t - ((int)gridDim.x - F) : -1;
+  }
+  __syncthreads();
+  if (s_finish < 0) return;
+  if (threadIdx.x == 0) {
+    const unsigned long long t0 = globaltimer_ns();
+    for (long n = 0; ld_acquire(r.hdr + kHdrRouterTicket) < (int)gridDim.x; ++n) {
+      if (n > (1l << 22) || globaltimer_ns() - t0 > 200ull * 1000 * 1000) {
+        atomicExch(r.hdr + kHdrStatus, MOE_ERR_DEVICE_TIMEOUT);
+        break;
+      }
+      __nanosleep(32);
     }
-    __syncthreads();
-  };
-  gemv_streamk<TT>(d, epi, on_tile);
-  if (s_finish) router_finish(r, d.M);
+  }
+  __syncthreads();
+  route_tokens(r, d.M, s_finish, F);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_finish = atomicAdd(r.hdr + kHdrRouterFin, 1) == F - 1;
+  }
+  __syncthreads();
+  if (!s_finish) return;
+  __threadfence();
+  route_order(r, d.M);
 }
 
 Gemv make_gemv(const GemvPlan& p, const void* A, const void* W, float* partials, unsigned* tickets) {

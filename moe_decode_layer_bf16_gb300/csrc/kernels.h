@@ -12,13 +12,14 @@ constexpr int kBlock = 128;  // weight scale block side / activation group lengt
 enum HdrWord {
   kHdrStatus = 0,        // 0 or MOE_ERR_DEVICE_TIMEOUT (sticky until read)
   kHdrFault = 1,         // test hook: withhold the first slot's ready signal
-  kHdrRouterTicket = 2,  // tiles of router logits reduced so far
+  kHdrRouterTicket = 2,  // router CTAs whose logits are complete
   kHdrQueue = 3,         // expert-kernel work queue head
   kHdrActive = 4,        // number of routed experts with at least one route
   kHdrDoneA = 5,         // w13 items finished (h stored and, when due, its group quantised)
   kHdrXReady = 6,        // router CTAs that have quantised their share of x (and, CTA 0, reset
                          // the expert kernel's counters); the expert kernel's last CTA clears it
   kHdrExit = 7,          // expert-kernel CTAs finished
+  kHdrRouterFin = 8,     // router CTAs that have routed their share of the tokens
   kHdrWords = 64
 };
 constexpr int kMaxRouterTickets = 1024;
