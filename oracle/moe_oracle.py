@@ -347,9 +347,18 @@ def moe_decode_layer(layer: Layer, x_bf16, residual_bf16, tokens=None):
     M, H = x_bf16.shape
     k = layer.top_k
     E = layer.num_experts
-    logits, scores, sel, ids, w = route(x_bf16, layer.router_w, layer.sel_bias, k,
-                                        layer.routed_scaling)
-    sorted_routes, offsets = route_order(ids, E)
+    if E == 0:
+        # a dense layer ([decode page] LayerStages._build_dense: a dense MLP as
+        # GEMVs, the shared-expert path with no router): no routes at all
+        k = 0
+        logits = scores = sel = np.zeros((M, 0))
+        ids = np.zeros((M, 0), np.int64)
+        w = np.zeros((M, 0))
+        sorted_routes, offsets = np.zeros(0, np.int64), np.zeros(1, np.int64)
+    else:
+        logits, scores, sel, ids, w = route(x_bf16, layer.router_w, layer.sel_bias, k,
+                                            layer.routed_scaling)
+        sorted_routes, offsets = route_order(ids, E)
     if tokens is None:
         tokens = np.arange(M)
     tokens = np.asarray(tokens, np.int64)

@@ -323,3 +323,22 @@ def test_mtp_front_halves_order_gather_and_norm():
     # gains multiply elementwise after the normalisation: a gain of 2 doubles the half
     _, ye2 = orc.mtp_front(ids, embed, hidden, 2 * ones, ones, 1e-6, np.concatenate([eye, zero], axis=1))
     assert np.array_equal(ye2, 2 * ye)
+
+
+def test_dense_layer_is_the_moe_layer_without_routed_weight():
+    # the dense path (no router, no experts) against the MoE path whose routed
+    # contribution is scaled away (routed_scaling = 0): same shared expert, same
+    # boundary, so the outputs must agree exactly
+    from moe_decode_layer_bf16_gb300 import synth
+    from moe_decode_layer_bf16_gb300.dims import TINY
+    lw = synth.make_layer(TINY, seed=3)
+    x, res = synth.make_tokens(5, TINY.hidden, seed=3)
+    L = oracle_layer(TINY.with_(routed_scaling=0.0), lw)
+    moe = orc.moe_decode_layer(L, to_np(x), to_np(res))
+    dense = orc.Layer(router_w=np.zeros((0, TINY.hidden)), sel_bias=None, w13=None, w13_s=None, w2=None,
+                      w2_s=None, sw13=L.sw13, sw13_s=L.sw13_s, sw2=L.sw2, sw2_s=L.sw2_s, gain=L.gain,
+                      top_k=0, routed_scaling=0.0, swiglu_limit=L.swiglu_limit, rms_eps=L.rms_eps,
+                      e8m0=L.e8m0)
+    d = orc.moe_decode_layer(dense, to_np(x), to_np(res))
+    assert np.array_equal(d["out"], moe["out"]) and np.array_equal(d["residual_out"], moe["residual_out"])
+    assert d["ids"].shape == (5, 0) and np.any(d["out"] != 0)
