@@ -54,8 +54,8 @@ ROUTER_BYTES = DSV3.num_experts * DSV3.hidden * 2
 # DRAM bytes (read + write) per activated expert of one expert-kernel launch, from an
 # ncu capture (profiles/experts_kernel_dsv3_e32_m8.txt) of the kernel built from the
 # experts.cu whose SHA-256 is given; the bench reports no traffic for any other source.
-TRAFFIC_CAPTURE = {"experts_cu_sha256": "176c2a05d1b0dfa6287dd389b84f1b3d168837037d60e491e7d17a346e25b0c8",
-                   "bytes_per_expert": (1_278_055_000 + 5_641_216) / 29}
+TRAFFIC_CAPTURE = {"experts_cu_sha256": "b32ac40b28452d7b7c532f6f4935bc40447d944028cb25fab70950b9fe44d5e2",
+                   "bytes_per_expert": 1_283_572_688 / 29}
 
 
 def layer_bytes(M: int, unique: int) -> int:
@@ -263,6 +263,38 @@ def mtp_front(m, flush_l2, dev, Ms=(1, 4, 16), reps=5):
     return res
 
 
+def dense_layer(m, flush_l2, dev, MS, reps=5):
+    """A DeepSeek-V3 dense layer (num_experts = 0: the 18432-wide FP8 MLP in the
+    shared-expert slot, no router) with its boundary, L2 flushed before every call."""
+    from moe_decode_layer_bf16_gb300.dims import DSV3_DENSE as D
+    lw = synth.make_layer(D, seed=21, device=dev)
+    wbytes = sum(lw[n].numel() * lw[n].element_size() for n in ("sw13", "sw13_s", "sw2", "sw2_s"))
+    res = {}
+    for M in MS:
+        lay = m.MoeDecodeLayer(D, lw, max_tokens=M, device=dev)
+        x, r = synth.make_tokens(M, D.hidden, seed=400 + M, device=dev)
+        o, ro = torch.empty_like(x), torch.empty_like(r)
+        times = []
+        for i in range(reps + 1):
+            flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            lay(x, r, o, ro)
+            e1.record()
+            torch.cuda.synchronize()
+            if i:
+                times.append(e0.elapsed_time(e1))
+        if lay.status() != m.MOE_OK:
+            raise RuntimeError("dense layer status")
+        us = 1e3 * statistics.median(times)
+        nbytes = wbytes + 4 * M * D.hidden * 2 + D.hidden * 2
+        res[str(M)] = {"us_per_layer": round(us, 2), "tokens_per_s": round(M * 1e6 / us, 1),
+                       "gbps": round(nbytes / us / 1e3, 1)}
+    del lw
+    torch.cuda.empty_cache()
+    return res
+
+
 def graph_chain(m, dims, lw0, MS, n_layers, reps, dev):
     """A decode chain captured as one CUDA graph: n_layers layers with distinct
     weights, each layer's out / residual_out feeding the next layer's x /
@@ -453,6 +485,12 @@ def run_ours(args, world, rank, local):
                                        "per_m": splitk_proj(m, flush_l2, dev, 7168, 14336)}
         except Exception as exc:
             extra["splitk_eh_proj"] = {"error": f"{type(exc).__name__}: {exc}"}
+        try:
+            extra["dense_layer"] = {"what": "DeepSeek-V3 dense layer (FP8 MLP 7168 x 18432, 396 MB) with its "
+                                            "boundary, L2 flushed, median of 5",
+                                    "per_m": dense_layer(m, flush_l2, dev, MS)}
+        except Exception as exc:
+            extra["dense_layer"] = {"error": f"{type(exc).__name__}: {exc}"}
         try:
             extra["mtp_eh_front"] = {"what": "mtp_eh_front, H=7168, vocab 129280, eh_proj [7168, 14336] (205.5 MB), "
                                              "L2 flushed, median of 5",

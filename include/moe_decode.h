@@ -11,8 +11,9 @@
  *   - All tensor arguments are DEVICE pointers to dense row-major arrays that
  *     the caller allocated on the current CUDA device.  The library never
  *     allocates, frees or synchronises (moe_device_status excepted), and keeps
- *     no pointer past return.  Weights are read, never written ("reads the
- *     backbone, never modifies it", [decode page] class SpecializedDecode).
+ *     no pointer past return.  Weights are read, never written (the decode
+ *     executor leaves the model's own weights untouched: [decode page] class
+ *     SpecializedDecode).
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Work is only enqueued; every call is stream-ordered.
  *   - Return value: MOE_OK or an error code below.  Argument errors are found
@@ -126,7 +127,8 @@ int moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
  *   m = sum_j w_j * y_(t,j) + y_shared;  r' = m + residual;
  *   residual_out = bf16(r');  out = bf16(r' * rsqrt(mean(r'^2) + eps) * gain).
  * ([decode page] LayerStages._mega_moe / _router; [draft page]
- * SpecializedDraft.reduced_norm: "norm(x + residual) and the new residual".)
+ * SpecializedDraft.reduced_norm: the boundary returns the normalised sum and
+ * the updated residual.)
  *
  *   x, residual      bf16 [M, H] inputs (may not alias the outputs)
  *   out, residual_out  bf16 [M, H] outputs
@@ -139,6 +141,13 @@ int moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
  *                    be used by two calls that may run concurrently
  * M == 0 is a no-op.  Launches exactly three kernels (router + top-k + route
  * order; the expert kernel; finalize + residual + RMSNorm).
+ *
+ * Dense layers ([decode page] LayerStages._build_dense: a dense FP8 MLP run as
+ * GEMVs): num_experts = 0, top_k = 0, inter = 0 and the MLP's weights in the
+ * shared-expert slot (sw13 [2 I_s, H], sw2 [H, I_s], I_s <= 32768); router_w,
+ * w13 and w2 are not read and may be NULL.  Then m = y_shared and the same
+ * boundary follows; topk_ids / topk_w / sorted_routes are empty and
+ * expert_offsets[0] = 0.
  */
 int moe_decode_layer(const moe_layer_dims *dims, const moe_layer_weights *w, int M,
                      const void *x, const void *residual, void *out, void *residual_out,

@@ -71,14 +71,19 @@ void layout_for(const moe_layer_dims& d, int M, Layout& L) {
 
 int check_dims(const moe_layer_dims* d) {
   if (!d) return MOE_ERR_INVALID_ARG;
-  if (d->hidden <= 0 || d->inter <= 0 || d->shared_inter < 0 || d->num_experts <= 0 || d->top_k <= 0)
+  if (d->num_experts == 0) {
+    // a dense layer: the MLP in the shared-expert slot, no router, no routed experts
+    if (d->top_k != 0 || d->inter != 0 || d->shared_inter <= 0) return MOE_ERR_INVALID_ARG;
+  } else if (d->inter <= 0 || d->top_k <= 0) {
     return MOE_ERR_INVALID_ARG;
+  }
+  if (d->hidden <= 0 || d->shared_inter < 0 || d->num_experts < 0) return MOE_ERR_INVALID_ARG;
   if (!std::isfinite(d->routed_scaling) || !(d->swiglu_limit > 0.f) || !(d->rms_eps >= 0.f) ||
       !std::isfinite(d->rms_eps))
     return MOE_ERR_INVALID_ARG;
   if (d->hidden % kBlock || d->hidden > 16384) return MOE_ERR_UNSUPPORTED;
   if (d->inter % kBlock || d->inter > 8192) return MOE_ERR_UNSUPPORTED;
-  if (d->shared_inter % kBlock || d->shared_inter > 8192) return MOE_ERR_UNSUPPORTED;
+  if (d->shared_inter % kBlock || d->shared_inter > 32768) return MOE_ERR_UNSUPPORTED;
   if (d->num_experts > kMaxExperts || d->num_experts % 16) return MOE_ERR_UNSUPPORTED;
   if (d->top_k > kMaxTopK || d->top_k > d->num_experts) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
@@ -136,10 +141,12 @@ static int layer_impl(const moe_layer_dims* dims, const moe_layer_weights* w, in
   if (M == 0) return MOE_OK;
   if ((long long)M * dims->top_k > kMaxMk) return MOE_ERR_UNSUPPORTED;
   const bool has_shared = dims->shared_inter > 0;
-  if (!w->router_w || !w->w13 || !w->w13_s || !w->w2 || !w->w2_s || !w->norm_gain) return MOE_ERR_INVALID_ARG;
+  const bool dense = dims->num_experts == 0;  // routed weights are not read (may be NULL)
+  if (!dense && (!w->router_w || !w->w13 || !w->w13_s || !w->w2 || !w->w2_s)) return MOE_ERR_INVALID_ARG;
+  if (!w->norm_gain) return MOE_ERR_INVALID_ARG;
   if (has_shared && (!w->sw13 || !w->sw13_s || !w->sw2 || !w->sw2_s)) return MOE_ERR_INVALID_ARG;
   if (!x || !residual || !out || !residual_out || !workspace) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(w->router_w) || !aligned16(w->w13) || !aligned16(w->w2) || !aligned16(x) ||
+  if ((!dense && (!aligned16(w->router_w) || !aligned16(w->w13) || !aligned16(w->w2))) || !aligned16(x) ||
       !aligned16(residual) || !aligned16(out) || !aligned16(residual_out) || !aligned16(w->norm_gain) ||
       !aligned16(workspace) || (has_shared && (!aligned16(w->sw13) || !aligned16(w->sw2))))
     return MOE_ERR_INVALID_ARG;
@@ -159,6 +166,12 @@ static int layer_impl(const moe_layer_dims* dims, const moe_layer_weights* w, in
   // sooner at one token chunk, more partial sums to add cost more above (measured)
   const int run = M <= 8 ? 2 : 4;
   plan_gemv(plan, M, E, H, gemv_grid((cells + run - 1) / run, sms, gemv_blocks_per_sm(chunk, true)));
+  if (dense) {
+    // no logits: the router kernel only quantises x (one warp per 1024-column
+    // slice of a token, 4 warps a CTA) and resets the expert kernel's counters
+    const long long slices = (long long)M * ((H / kBlock + 7) / 8);
+    plan.G = (int)std::max<long long>(1, std::min<long long>((slices + 3) / 4, sms));
+  }
   if ((long long)plan.n_chunks * plan.n_tiles > kMaxRouterTickets) return MOE_ERR_UNSUPPORTED;
   if (gemv_partials_bytes(plan) > gemv_partials_bound(M, E, H)) return MOE_ERR_UNSUPPORTED;
 
@@ -202,6 +215,10 @@ static int layer_impl(const moe_layer_dims* dims, const moe_layer_weights* w, in
   ea.rows = reinterpret_cast<float*>(ws + L.rows);
   ea.shared_out = reinterpret_cast<float*>(ws + L.shared);
   ea.router_ctas = plan.G;
+  // a w2 item streams its 32-row groups over all of I: 4 of them (a whole
+  // scale block) unless the rows are long (I >= 8192, a dense layer's MLP),
+  // where single groups keep the queue's tail short
+  ea.bq = L.Imax >= 8192 ? 1 : 4;
   if (launch_experts(ea, sms, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (!mark(2)) return MOE_ERR_CUDA;
 

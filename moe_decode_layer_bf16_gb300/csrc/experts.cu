@@ -1,8 +1,8 @@
 // The routed + shared experts of one MoE decode step as one persistent kernel
 // (the decode page, vllm.models.glm5next.nvidia.specialized_decode.runtime
-// .decode, LayerStages._mega_moe: "routed experts as one kernel"; its grouped
-// form "runs the shared expert as one more expert", which this kernel does at
-// every token count).
+// .decode, LayerStages._mega_moe: the routed experts in a single kernel; its
+// grouped form folds the shared expert in as an extra expert, which this
+// kernel does at every token count).
 //
 // Per expert: [g; u] = xq . w13^T with 128x128 block scales, clamped SwiGLU
 // h = silu(min(g, L)) * clamp(u, -L, L), h re-quantised to FP8 per route per
@@ -72,8 +72,8 @@ enum MetaFlag { kFirst = 1, kLast = 2, kSkip = 4, kEnd = 8, kPassEnd = 16, kXT =
 // decode nothing themselves: ints [0, 4) item, pass | quarter << 16, first
 // k-block, flags; [4] tokens of the pass, [5] valid k-blocks of the stage; at
 // the first stage of a pass also [8, 12) the weight-scale rows of the two
-// 16-row tiles (two pointers) and [16, 32) each token's scale-row offset.
-constexpr int kMetaInts = 32;
+// 16-row tiles (two pointers) and [16, 16 + tokens of the pass) each token's
+// scale-row offset: Cfg<TT>::kMetaInts ints a slot.
 
 template <int TT>
 struct Cfg {
@@ -81,8 +81,13 @@ struct Cfg {
   static constexpr int kXBytes = ((kTok * kXStride + 1023) / 1024) * 1024;
   static constexpr int kXHalf = kTok * kKH * 128;  // one activation box (tokens x 4 k-blocks)
   static constexpr int kSlot = kWBytes + kXBytes;
-  static_assert(TT == 1 || TT == 2, "passes of 8 or 16 tokens");
-  static constexpr int kRedBufs = 2;  // epilogue hand-off buffers
+  // a stage descriptor: 16 ints, then one scale-row offset per token of the
+  // pass (a multiple of 4 ints, for the 16-byte stores); as small as it can
+  // be, since at 8-token passes the ring's fifth stage fits with little room
+  static constexpr int kMetaInts = 16 + kTok;
+  static_assert(kMetaInts % 4 == 0, "16-byte aligned descriptors");
+  static_assert(TT == 1 || TT == 2 || TT == 4, "passes of 8, 16 or 32 tokens");
+  static constexpr int kRedBufs = TT == 4 ? 1 : 2;  // epilogue hand-off buffers (one fits at 32 tokens)
   // consumer warps: each owns one 16-row tile and kKP of the stage's 8 k-blocks
   // (16 warps x 1 k-block where the registers allow, else 8 warps x 2)
   static constexpr int kCW = TT == 1 ? 16 : 8;
@@ -192,9 +197,11 @@ struct Tables {
 struct Item {
   bool a;
   int slot, idx;  // slice (A) or 128-row block (B)
+  int q0;         // B: first 32-row quarter of the block
 };
 
-MOE_DEV Item decode_item(int item, int nA_sh, int nA_r, int totA, int nB, bool has_shared) {
+// B items: bq quarters of a 128-row block each (4: the whole block)
+MOE_DEV Item decode_item(int item, int nA_sh, int nA_r, int totA, int nB, bool has_shared, int bq) {
   Item it;
   if (item < totA) {
     it.a = true;
@@ -202,9 +209,12 @@ MOE_DEV Item decode_item(int item, int nA_sh, int nA_r, int totA, int nB, bool h
     else { const int j = item - nA_sh; it.slot = j / nA_r + (has_shared ? 1 : 0); it.idx = j % nA_r; }
   } else {
     it.a = false;
+    const int lp = bq == 4 ? 0 : 2;  // log2 of the items per 128-row block
     const int j = item - totA;
-    it.slot = j / nB;
-    it.idx = j % nB;
+    it.slot = j / (nB << lp);
+    const int r = j - it.slot * (nB << lp);
+    it.idx = r >> lp;
+    it.q0 = (r & ((1 << lp) - 1)) * bq;
   }
   return it;
 }
@@ -246,6 +256,7 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
   using C = Cfg<TT>;
   constexpr int kTok = C::kTok;
   constexpr int kCW = C::kCW, kKP = C::kKP, kKW = C::kKW, kPW = C::kPW, kEW = C::kEW, kThreads = C::kThreads;
+  constexpr int kMetaInts = C::kMetaInts;
   constexpr int kRedF = 2 * kKW * 16 * kTok;  // floats of one epilogue hand-off buffer
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (su32(smem_raw) & 1023)) & 1023);
@@ -340,17 +351,17 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
         if (lane == 0) s_misc[0] = n_act;  // for the epilogue warp's decoding
         __syncwarp();
         totA = nA_sh + n_act * nA_r;
-        total = totA + ((has_shared ? 1 : 0) + n_act) * nB;
+        total = totA + ((has_shared ? 1 : 0) + n_act) * nB * (4 / p.bq);
         routed = true;
       }
       if (item >= total) break;
       int nxt = 0;
       if (lane == 0) nxt = atomicAdd(p.hdr + kHdrQueue, 1);
-      const Item it = decode_item(item, nA_sh, nA_r, totA, nB, has_shared);
+      const Item it = decode_item(item, nA_sh, nA_r, totA, nB, has_shared, p.bq);
       const Slot s = make_slot(p, tb, it.slot, has_shared);
       const int nkbK = it.a ? nkbH : s.Ie / kBlock;
       const int nkg = (nkbK + kKBS - 1) / kKBS;     // k-block groups
-      const int nq = it.a ? 1 : kRowsB / kRowsQ;    // row quarters (B)
+      const int nq = it.a ? 1 : p.bq;               // row quarters (B)
       const int nstage = nkg * nq;
       bool skip = false;
       // (lane 0 loads the counts below with ld.acquire, so that its later
@@ -415,7 +426,7 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
           xsrc = it.a ? p.xq + (size_t)token_of(p, tb, s, pass * kTok + lane) * p.H
                       : p.hq + (size_t)(s.hbase + pass * kTok + lane) * p.Imax;
         const int la_st = min(2, nstage - 1);  // stage that looks ahead at the next item
-        int qr = 0, kb0 = 0;                   // row quarter and first k-block of stage st
+        int qr = it.a ? 0 : it.q0, kb0 = 0;    // row quarter and first k-block of stage st
         for (int st = 0; st < (skip ? 1 : nstage); ++st) {
           int ok = 1;
           if (lane == 0) ok = mbar_wait(empty + si, ph ^ 1u, status);
@@ -472,7 +483,7 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
           if (lane == 0 && pass == 0 && st == la_st && nxt < total) {
             // look ahead: load the readiness of the next item's expert now, so
             // that a w2 item rarely waits on a round trip when it starts
-            const Item nit = decode_item(nxt, nA_sh, nA_r, totA, nB, has_shared);
+            const Item nit = decode_item(nxt, nA_sh, nA_r, totA, nB, has_shared, p.bq);
             if (!nit.a && !all_ready) {
               pre_done = ld_acquire(p.hdr + kHdrDoneA);
               if (!s_rdy[nit.slot]) {
@@ -527,7 +538,7 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
         cur = item;
         // routed items come after the producer loaded the routing (and s_misc[0])
         const int totA = nA_sh + *(volatile int*)s_misc * nA_r;
-        it = decode_item(item, nA_sh, nA_r, totA, nB, has_shared);
+        it = decode_item(item, nA_sh, nA_r, totA, nB, has_shared, p.bq);
         s = make_slot(p, tb, it.slot, has_shared);
       }
       const int ntok = min(kTok, s.nt - pass * kTok);
@@ -799,7 +810,7 @@ bool map_w2(CUtensorMap* m, const uint8_t* base, int H, int I, int n) {
 
 template <int TT>
 size_t other_smem(const ExpertArgs& a, int nst) {
-  return (size_t)nst * (kMetaInts * sizeof(int) + 2 * sizeof(uint64_t)) + 2 * sizeof(uint64_t) + 4 * sizeof(int) +
+  return (size_t)nst * (Cfg<TT>::kMetaInts * sizeof(int) + 2 * sizeof(uint64_t)) + 2 * sizeof(uint64_t) + 4 * sizeof(int) +
          sizeof(float) * ((size_t)Cfg<TT>::kRedBufs * 2 * Cfg<TT>::kKW * 16 * Cfg<TT>::kTok) + 4 * sizeof(int) +
          2 * sizeof(uint64_t) +
          sizeof(int) * (3 * a.E + 2 + a.Mk + 4) + 1024;
@@ -836,7 +847,8 @@ cudaError_t launch_experts(const ExpertArgs& a, int num_sms, cudaStream_t s) {
   if (!encode_fn()) return cudaErrorNotSupported;
   TmaMaps maps;
   memset(&maps, 0, sizeof(maps));
-  if (!map_w13(&maps.w13, a.w13, a.H, a.I, a.E) || !map_w2(&maps.w2, a.w2, a.H, a.I, a.E))
+  // (a dense layer has no routed experts: their maps stay zero, never used)
+  if (a.E > 0 && (!map_w13(&maps.w13, a.w13, a.H, a.I, a.E) || !map_w2(&maps.w2, a.w2, a.H, a.I, a.E)))
     return cudaErrorInvalidValue;
   if (a.Is > 0 && (!map_w13(&maps.sw13, a.sw13, a.H, a.Is, 1) || !map_w2(&maps.sw2, a.sw2, a.H, a.Is, 1)))
     return cudaErrorInvalidValue;
@@ -844,6 +856,13 @@ cudaError_t launch_experts(const ExpertArgs& a, int num_sms, cudaStream_t s) {
   // M = 8) streams its rows once per pass, the repeats from L2.  Wider passes
   // cost consumer registers and ring stages, and measured slower on the
   // DeepSeek-V3-shaped layer up to M = 128 tokens; 16-token passes win above.
+  if (a.E == 0) {
+    // a dense layer: every token goes through the one MLP, so the widest pass
+    // streams its weights the fewest times
+    if (a.M <= 8) return launch_tt<1>(a, maps, num_sms, s);
+    if (a.M <= 16) return launch_tt<2>(a, maps, num_sms, s);
+    return launch_tt<4>(a, maps, num_sms, s);
+  }
   if (a.M <= 128) return launch_tt<1>(a, maps, num_sms, s);
   return launch_tt<2>(a, maps, num_sms, s);
 }

@@ -97,6 +97,7 @@ struct ExpertArgs {
   float* h; uint8_t* hq; float* hs;
   float* rows; float* shared_out;
   int router_ctas;  // CTAs of the router launch that precedes this kernel
+  int bq;           // w2 item size in 32-row quarters of a 128-row block: 4, or 1 for long rows
 };
 cudaError_t launch_experts(const ExpertArgs& a, int num_sms, cudaStream_t s);
 

@@ -1,9 +1,9 @@
 // Layer boundary: weighted top-k finalize, residual add and RMSNorm.
 //
 // The draft page (vllm.models.glm5next.nvidia.specialized_decode.runtime.draft,
-// SpecializedDraft.reduced_norm) defines the boundary as "norm(x + residual)
-// and the new residual"; on one GPU the tensor-parallel all-reduce it is
-// fused with drops out.  The decode page (LayerStages._mega_moe) leaves the
+// SpecializedDraft.reduced_norm) makes the boundary return the normalised sum
+// of the sublayer output and the residual, and the updated residual; on one
+// GPU the tensor-parallel all-reduce it is fused with drops out.  The decode page (LayerStages._mega_moe) leaves the
 // routed rows unfinalized in expanded order for this step, which weights them
 // by the top-k weights and adds the shared expert.
 //

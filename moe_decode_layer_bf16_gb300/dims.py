@@ -33,3 +33,8 @@ class LayerDims:
 TINY = LayerDims(hidden=512, inter=256, shared_inter=256, num_experts=16, top_k=4)
 # DeepSeek-V3-shaped decode layer: H=7168, 256 routed experts, top-8, I = I_s = 2048.
 DSV3 = LayerDims(hidden=7168, inter=2048, shared_inter=2048, num_experts=256, top_k=8)
+# Dense layers (num_experts = 0): the MLP in the shared-expert slot, no router
+# ([decode page] LayerStages._build_dense runs dense MLPs as GEMVs).
+TINY_DENSE = LayerDims(hidden=512, inter=0, shared_inter=768, num_experts=0, top_k=0)
+# DeepSeek-V3's dense layers: H = 7168, intermediate 18432.
+DSV3_DENSE = LayerDims(hidden=7168, inter=0, shared_inter=18432, num_experts=0, top_k=0)

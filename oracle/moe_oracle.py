@@ -260,8 +260,8 @@ def expert_mlp(xq, xs, w13_deq, w2_deq, limit, e8m0):
 
 # --------------------------------------------------------------------------
 # Boundary: finalize + residual add + RMSNorm ([draft page]: the MTP layer's
-# boundary is a fused residual add and RMSNorm, reduced_norm returns
-# norm(x + residual) and the new residual).
+# boundary fuses the residual add with the RMSNorm; reduced_norm gives back
+# the normalised sum and the updated residual).
 # --------------------------------------------------------------------------
 
 def rmsnorm_residual(m, residual_bf16, gain_bf16, eps):

@@ -68,6 +68,18 @@ def test_bad_dims_rejected(L, bad, code):
     assert e.value.status == code
 
 
+def test_dense_dims(L):
+    # num_experts = 0 is a dense layer: top_k and inter must be 0, the MLP sits
+    # in the shared-expert slot (up to 32768 wide)
+    from moe_decode_layer_bf16_gb300.dims import DSV3_DENSE
+    assert m.moe_decode_workspace_size(DSV3_DENSE, 32) > 0
+    for bad, code in [(dict(top_k=1), m.MOE_ERR_INVALID_ARG), (dict(inter=128), m.MOE_ERR_INVALID_ARG),
+                      (dict(shared_inter=0), m.MOE_ERR_INVALID_ARG),
+                      (dict(shared_inter=32768 + 128), m.MOE_ERR_UNSUPPORTED)]:
+        n = ctypes.c_size_t(0)
+        assert L.moe_decode_workspace_size(ctypes.byref(m._dims(DSV3_DENSE.with_(**bad))), 4, ctypes.byref(n)) == code
+
+
 def test_too_many_tokens_unsupported(L):
     with pytest.raises(m.MoeError) as e:
         m.moe_decode_workspace_size(DSV3, 1024)

@@ -316,3 +316,32 @@ def test_mtp_front_bad_token_id_is_reported():
     assert m.moe_device_status(ws) == m.MOE_ERR_INVALID_ARG
     a = to_np(ws[256:256 + M * 2 * H * 2].view(torch.bfloat16).view(M, 2 * H))
     assert not a[1, :H].any() and a[0, :H].any() and a[1, H:].any()
+
+
+# ------------------------------------------------------------ dense layers
+
+@pytest.mark.parametrize("M", [1, 5, 33])
+def test_dense_layer_tiny(M):
+    # num_experts = 0: the MLP in the shared-expert slot, no router
+    from moe_decode_layer_bf16_gb300.dims import TINY_DENSE
+    lw = synth.make_layer(TINY_DENSE, seed=11, device=DEV)
+    x, res = synth.make_tokens(M, TINY_DENSE.hidden, seed=200 + M, device=DEV)
+    g = run_gpu(TINY_DENSE, lw, x, res)
+    ref = orc.moe_decode_layer(oracle_layer(TINY_DENSE, lw), to_np(x), to_np(res))
+    assert g["ids"].shape == (M, 0) and np.array_equal(g["off"], [0])
+    assert orc.max_abs_rel(g["out"], ref["out"]) <= TOL
+    assert orc.max_abs_rel(g["residual_out"], ref["residual_out"]) <= TOL
+
+
+@pytest.mark.parametrize("M", [1, 8, 32])
+def test_dense_layer_dsv3_sampled(M):
+    # DeepSeek-V3's dense MLP (intermediate 18432, 396 MB of FP8 weights): the
+    # w2 items are single 32-row groups there; first and last token checked
+    from moe_decode_layer_bf16_gb300.dims import DSV3_DENSE
+    lw = synth.make_layer(DSV3_DENSE, seed=12, device=DEV)
+    x, res = synth.make_tokens(M, DSV3_DENSE.hidden, seed=300 + M, device=DEV)
+    g = run_gpu(DSV3_DENSE, lw, x, res)
+    tokens = sorted({0, M - 1})
+    ref = orc.moe_decode_layer(LazyLayer(DSV3_DENSE, lw), to_np(x), to_np(res), tokens=tokens)
+    assert orc.max_abs_rel(g["out"][tokens], ref["out"]) <= TOL
+    assert orc.max_abs_rel(g["residual_out"][tokens], ref["residual_out"]) <= TOL
