@@ -28,6 +28,7 @@ for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
 
 import argparse
 import hashlib
+import re
 import json
 import statistics
 import subprocess
@@ -53,9 +54,18 @@ EXPERT_BYTES = 2 * DSV3.inter * DSV3.hidden + DSV3.hidden * DSV3.inter + 4 * (
 ROUTER_BYTES = DSV3.num_experts * DSV3.hidden * 2
 # DRAM bytes (read + write) per activated expert of one expert-kernel launch, from an
 # ncu capture (profiles/experts_kernel_dsv3_e32_m8.txt) of the kernel built from the
-# experts.cu whose SHA-256 is given; the bench reports no traffic for any other source.
-TRAFFIC_CAPTURE = {"experts_cu_sha256": "b32ac40b28452d7b7c532f6f4935bc40447d944028cb25fab70950b9fe44d5e2",
+# experts.cu whose code (comments and white space removed) has the SHA-256 given; the
+# bench reports no traffic for any other code.
+TRAFFIC_CAPTURE = {"experts_cu_code_sha256": "6288ac9160798982cc49b3911d7ba16defbcf798c97f76b4bc6c1cf98969a3c7",
                    "bytes_per_expert": 1_283_572_688 / 29}
+
+
+def code_sha256(path):
+    """SHA-256 of a CUDA source with its comments and white space removed."""
+    src = open(path).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return hashlib.sha256(re.sub(r"\s+", "", src).encode()).hexdigest()
 
 
 def layer_bytes(M: int, unique: int) -> int:
@@ -441,7 +451,7 @@ def run_ours(args, world, rank, local):
     achieved = exp_bytes_all / (exp_ms_all / 1e3) / 1e9
     traffic = None
     src = os.path.join(ROOT, "moe_decode_layer_bf16_gb300", "csrc", "experts.cu")
-    if hashlib.sha256(open(src, "rb").read()).hexdigest() == TRAFFIC_CAPTURE["experts_cu_sha256"]:
+    if code_sha256(src) == TRAFFIC_CAPTURE["experts_cu_code_sha256"]:
         # per launch, averaged over the launches like `achieved`
         traffic = round(TRAFFIC_CAPTURE["bytes_per_expert"] * sum(unique[M] + 1 for M in MS) / len(MS))
     for M in MS:

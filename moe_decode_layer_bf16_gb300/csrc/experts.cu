@@ -20,10 +20,10 @@
 //     shared expert first, then all w2 items):
 //       A item (expert, 16 intermediates): 16 gate + 16 up rows of w13 over H,
 //       B item (expert, 128 rows of w2, one scale block) over I, streamed as
-//       four 32-row groups;
+//       four 32-row groups (one group per item when I is long: a dense MLP);
 //   * a stage is 8 k-blocks (1024 columns): two 16 KB TMA boxes of weights
 //     (128-byte swizzle) plus the pass's FP8 activation columns (TMA boxes of
-//     contiguous rows, or one 1-D bulk copy per gathered token row), all
+//     the shared expert's x rows, or one 1-D bulk copy per token row), all
 //     completing on the stage's mbarrier; the producer runs up to a whole
 //     ring of stages ahead, across item boundaries, so epilogues overlap the
 //     stream;
@@ -520,7 +520,7 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
     __syncwarp();
   } else if (warp == kEW) {
     // ================================================================ epilogue
-    // Adds the four k-block partial sums of each finished 32-row group, applies
+    // Adds the k-block partial sums of each finished 32-row group, applies
     // SwiGLU (w13) or stores the rows (w2), and runs the group counters and the
     // re-quantisation of h, so the consumer warps never wait on global atomics.
     uint32_t uses = 0;

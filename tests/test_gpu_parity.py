@@ -105,6 +105,21 @@ def test_layer_variants(name, M):
     compare(dims, lw, x, res)
 
 
+def test_zero_tokens_is_a_no_op():
+    lw = synth.make_layer(TINY, seed=2, device=DEV)
+    layer = m.MoeDecodeLayer(TINY, lw, max_tokens=4)
+    x = torch.empty((0, TINY.hidden), dtype=torch.bfloat16, device=DEV)
+    out = torch.empty_like(x)
+    layer(x, x, out, out)
+    torch.cuda.synchronize()
+    assert layer.status() == m.MOE_OK
+    # and the workspace still serves a real call afterwards
+    xs, res, _ = tie_free_tokens(TINY, lw, 3, seed=2, device=DEV)
+    g = run_gpu(TINY, lw, xs, res, layer)
+    ref = orc.moe_decode_layer(oracle_layer(TINY, lw), to_np(xs), to_np(res))
+    assert np.array_equal(g["ids"], ref["ids"]) and orc.max_abs_rel(g["out"], ref["out"]) <= TOL
+
+
 def test_outputs_are_deterministic():
     dims = TINY.with_(num_experts=64, top_k=8, hidden=1024)
     lw = synth.make_layer(dims, seed=3, device=DEV)
@@ -232,7 +247,8 @@ def dsv3_skewed():
     return dims, lw, LazyLayer(dims, lw)
 
 
-@pytest.mark.parametrize("M", [1, 8, 32, 64, 128, 256])
+# 512 tokens: M * k = 4096 routes, the largest step the workspace takes
+@pytest.mark.parametrize("M", [1, 8, 32, 64, 128, 256, 512])
 def test_dsv3_layer_sampled(dsv3, M):
     lw, L = dsv3
     x, res, _ = tie_free_tokens(DSV3, lw, M, seed=1000 + M, device=DEV)
