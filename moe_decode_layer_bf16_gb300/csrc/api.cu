@@ -226,6 +226,9 @@ static int layer_impl(const moe_layer_dims* dims, const moe_layer_weights* w, in
   na.x = nullptr; na.residual = residual; na.gain = w->norm_gain;
   na.rows = ea.rows; na.route_w = ra.tw; na.shared = has_shared ? ea.shared_out : nullptr;
   na.out = out; na.residual_out = residual_out; na.M = M; na.H = H; na.k = k; na.eps = dims->rms_eps;
+  // the residual and the gain were written before the router's plain launch,
+  // so the boundary may load them before it waits on the expert kernel
+  na.early = 1;
   if (launch_rmsnorm(na, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (!mark(3)) return MOE_ERR_CUDA;
   return MOE_OK;
@@ -296,6 +299,7 @@ int rmsnorm_residual(const void* x, const void* residual, const void* gain, int 
   na.x = x; na.residual = residual; na.gain = gain; na.rows = rows; na.route_w = route_w;
   na.shared = shared; na.out = out; na.residual_out = residual_out; na.M = M; na.H = H;
   na.k = rows ? k : 0; na.eps = eps;
+  na.early = 0;  // the preceding kernel may be the one that writes them
   return launch_rmsnorm(na, (cudaStream_t)stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -58,6 +58,7 @@ constexpr int kRowsQ = 32;                // w2 rows per stage (a quarter of a B
 constexpr int kWBytes = 32768;            // weight tile per stage (two 16 KB boxes)
 constexpr int kWHalf = 16384;
 constexpr int kXStride = 1088;            // gathered activation row pitch in a stage (1024 + 64)
+constexpr int kTabPer = 16;               // routing-table loads a producer lane keeps in flight
 constexpr int kSmemMax = 227 * 1024;
 constexpr unsigned long long kWaitNs = 200ull * 1000ull * 1000ull;
 
@@ -343,11 +344,31 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
     while (alive) {
       if (item >= nA_sh && !routed) {
         // the routing: the router grid has completed and its writes are visible
+        // The tables (offsets, active experts: at most min(E, Mk), route order)
+        // and the count come in one batch of independent loads: this hand-over
+        // is on the layer's critical path.
         grid_dep_wait();
-        const int n_act = *(volatile int*)(p.hdr + kHdrActive);
-        for (int i = lane; i <= p.E; i += 32) s_off[i] = p.off[i];
-        for (int i = lane; i < n_act; i += 32) s_act[i] = p.act[i];
-        for (int i = lane; i < p.Mk; i += 32) s_sorted[i] = p.sorted[i];
+        const int nOff = p.E + 1, nAct = min(p.E, p.Mk), nAll = nOff + nAct + p.Mk;
+        int n_act = 0;
+        if (lane == 0) n_act = __ldcg(p.hdr + kHdrActive);
+        for (int b0 = 0; b0 < nAll; b0 += 32 * kTabPer) {
+          int v[kTabPer];
+#pragma unroll
+          for (int j = 0; j < kTabPer; ++j) {
+            const int i = b0 + 32 * j + lane;
+            v[j] = i < nOff ? __ldcg(p.off + i)
+                 : i < nOff + nAct ? __ldcg(p.act + (i - nOff))
+                 : i < nAll ? __ldcg(p.sorted + (i - nOff - nAct)) : 0;
+          }
+#pragma unroll
+          for (int j = 0; j < kTabPer; ++j) {
+            const int i = b0 + 32 * j + lane;
+            if (i < nOff) s_off[i] = v[j];
+            else if (i < nOff + nAct) s_act[i - nOff] = v[j];
+            else if (i < nAll) s_sorted[i - nOff - nAct] = v[j];
+          }
+        }
+        n_act = __shfl_sync(0xffffffffu, n_act, 0);
         if (lane == 0) s_misc[0] = n_act;  // for the epilogue warp's decoding
         __syncwarp();
         totA = nA_sh + n_act * nA_r;

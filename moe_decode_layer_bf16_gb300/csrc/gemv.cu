@@ -279,8 +279,10 @@ constexpr int kMaxFinish = 8;  // CTAs that share the routing of the tokens
 
 // Top-k, routing weights and per-token outputs of the tokens of finisher f of
 // F: warp w takes tokens 4 f + w, 4 f + w + 4 F, ...  Each warp stages its
-// token's logits (written by other CTAs: read from L2) in shared memory.
-__device__ void route_tokens(const RouterDev& r, int M, int f, int F) {
+// token's logits (written by other CTAs: read from L2) in shared memory.  A
+// lone finisher (F = 1) also keeps the ids in shared memory (ids_sh) for the
+// route order it builds next.
+__device__ void route_tokens(const RouterDev& r, int M, int f, int F, int* ids_sh) {
   __shared__ __align__(16) float s_lg[kThreads / 32][kMaxExperts];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int k = r.k, E = r.E;
@@ -297,6 +299,7 @@ __device__ void route_tokens(const RouterDev& r, int M, int f, int F) {
     if (lane < k) {
       const float w = s / sum * r.scaling;
       r.ids[t * k + lane] = id;
+      if (ids_sh) ids_sh[t * k + lane] = id;
       r.tw[t * k + lane] = w;
       if (r.user_ids) r.user_ids[t * k + lane] = id;
       if (r.user_w) r.user_w[t * k + lane] = w;
@@ -305,16 +308,17 @@ __device__ void route_tokens(const RouterDev& r, int M, int f, int F) {
   }
 }
 
-// Route order from all tokens' ids (written by the finishers): histogram,
-// exclusive scans, the list of active experts and the stable placement.
-__device__ void route_order(const RouterDev& r, int M) {
-  __shared__ int s_ids[kMaxMk];
+// Route order from all tokens' ids (written by the finishers, or already in
+// s_ids when this CTA routed every token): histogram, exclusive scans, the
+// list of active experts and the stable placement.
+__device__ void route_order(const RouterDev& r, int M, int* s_ids, bool ids_in_smem) {
   __shared__ int s_cnt[kMaxExperts];
   __shared__ int s_cur[kMaxExperts];
   __shared__ int s_nact;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int k = r.k, Mk = M * k, E = r.E;
-  for (int i = threadIdx.x; i < Mk; i += kThreads) s_ids[i] = __ldcg(r.ids + i);
+  if (!ids_in_smem)
+    for (int i = threadIdx.x; i < Mk; i += kThreads) s_ids[i] = __ldcg(r.ids + i);
   for (int e = threadIdx.x; e < E; e += kThreads) s_cnt[e] = 0;
   __syncthreads();
   for (int i = threadIdx.x; i < Mk; i += kThreads) atomicAdd(&s_cnt[s_ids[i]], 1);
@@ -376,6 +380,7 @@ __device__ void route_order(const RouterDev& r, int M) {
 template <int TT>
 __global__ void __launch_bounds__(kThreads) router_kernel(Gemv d, RouterDev r) {
   __shared__ int s_finish;
+  __shared__ int s_ids[kMaxMk];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   grid_dep_launch();  // the expert kernel may be scheduled on SMs this grid leaves free
   // (1) FP8 quantisation of x, per token per 128-column group, and (CTA 0) the
@@ -438,9 +443,10 @@ __global__ void __launch_bounds__(kThreads) router_kernel(Gemv d, RouterDev r) {
   auto epi = [&](int n, int row, float v) { r.logits[(size_t)n * r.E + row] = v; };
   gemv_streamk<TT>(d, epi, [] {});
   // (3) the last F CTAs to finish their logits route the tokens (one warp per
-  // token), once every CTA's logits are in; the last of
-  // them builds the route order.  Every CTA of this grid is resident (it
-  // launches before the expert kernel can), so the wait ends; it is bounded.
+  // token), once every CTA's logits are in; the last of them (or the only one,
+  // from its own shared memory) builds the route order.  Every CTA of this
+  // grid is resident (it launches before the expert kernel can), so the wait
+  // ends; it is bounded.
   const int F = min(min(kMaxFinish, (d.M + 3) / 4), (int)gridDim.x);
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -461,16 +467,19 @@ __global__ void __launch_bounds__(kThreads) router_kernel(Gemv d, RouterDev r) {
     }
   }
   __syncthreads();
-  route_tokens(r, d.M, s_finish, F);
+  route_tokens(r, d.M, s_finish, F, F == 1 ? s_ids : nullptr);
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (F > 1) {
+    // the last finisher to be done orders the routes, from every finisher's ids
+    if (threadIdx.x == 0) {
+      __threadfence();
+      s_finish = atomicAdd(r.hdr + kHdrRouterFin, 1) == F - 1;
+    }
+    __syncthreads();
+    if (!s_finish) return;
     __threadfence();
-    s_finish = atomicAdd(r.hdr + kHdrRouterFin, 1) == F - 1;
   }
-  __syncthreads();
-  if (!s_finish) return;
-  __threadfence();
-  route_order(r, d.M);
+  route_order(r, d.M, s_ids, F == 1);
 }
 
 Gemv make_gemv(const GemvPlan& p, const void* A, const void* W, float* partials, unsigned* tickets) {

@@ -107,6 +107,7 @@ struct NormArgs {
   void* out; void* residual_out;
   int M, H, k;
   float eps;
+  int early;  // residual and gain come from before the preceding kernels (the layer call)
 };
 cudaError_t launch_rmsnorm(const NormArgs& a, cudaStream_t s);
 

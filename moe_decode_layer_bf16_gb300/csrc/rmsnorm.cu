@@ -25,14 +25,15 @@ namespace {
 constexpr int kCluster = 8;
 constexpr int kThreads = 256;
 constexpr int kMaxCols = 16384 / kCluster;
+constexpr int kIter = kMaxCols / (kThreads * 4);  // 4-column groups a thread handles
 
-__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
+// (two CTAs an SM: at 32 tokens the 256 CTAs then fit in one wave)
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 2)
     rmsnorm_kernel(NormArgs a) {
   __shared__ float s_rb[kMaxCols];
   __shared__ float s_warp[kThreads / 32];
   __shared__ float s_part;
   cg::cluster_group cluster = cg::this_cluster();
-  grid_dep_wait();  // the rows come from the preceding expert kernel
   const int rank = (int)cluster.block_rank();
   const int t = blockIdx.x / kCluster;
   const int ncol = a.H / kCluster, c0 = rank * ncol;
@@ -40,10 +41,31 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
   const size_t rowo = (size_t)t * a.H + c0;
   const uint16_t* res = reinterpret_cast<const uint16_t*>(a.residual) + rowo;
   const uint16_t* xx = a.x ? reinterpret_cast<const uint16_t*>(a.x) + rowo : nullptr;
+  const uint16_t* gain = reinterpret_cast<const uint16_t*>(a.gain) + c0;
   uint16_t* ro = reinterpret_cast<uint16_t*>(a.residual_out) + rowo;
+  // The residual and the gain: inside the layer call (early) neither comes
+  // from the kernels this one waits for, so they are loaded while those
+  // finish; a stand-alone call loads them after the wait, like x.
+  uint2 rv[kIter], gv[kIter];
+  auto load_inputs = [&] {
+#pragma unroll
+    for (int i = 0; i < kIter; ++i) {
+      const int j = tid * 4 + i * kThreads * 4;
+      if (j < ncol) {
+        rv[i] = *reinterpret_cast<const uint2*>(res + j);
+        gv[i] = *reinterpret_cast<const uint2*>(gain + j);
+      }
+    }
+  };
+  if (a.early) load_inputs();
+  grid_dep_wait();  // the rows come from the preceding expert kernel
+  if (!a.early) load_inputs();
 
   float ss = 0.f;
-  for (int j = tid * 4; j < ncol; j += kThreads * 4) {
+#pragma unroll
+  for (int i = 0; i < kIter; ++i) {
+    const int j = tid * 4 + i * kThreads * 4;
+    if (j >= ncol) break;
     float m[4] = {0.f, 0.f, 0.f, 0.f};
     if (xx) {
       const uint2 v = *reinterpret_cast<const uint2*>(xx + j);
@@ -71,9 +93,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
       const float4 r = *reinterpret_cast<const float4*>(a.shared + rowo + j);
       m[0] += r.x; m[1] += r.y; m[2] += r.z; m[3] += r.w;
     }
-    const uint2 rv = *reinterpret_cast<const uint2*>(res + j);
-    const float r0 = m[0] + bf16_lo(rv.x), r1 = m[1] + bf16_hi(rv.x);
-    const float r2 = m[2] + bf16_lo(rv.y), r3 = m[3] + bf16_hi(rv.y);
+    const float r0 = m[0] + bf16_lo(rv[i].x), r1 = m[1] + bf16_hi(rv[i].x);
+    const float r2 = m[2] + bf16_lo(rv[i].y), r3 = m[3] + bf16_hi(rv[i].y);
     const uint32_t p01 = pack_bf16(r0, r1), p23 = pack_bf16(r2, r3);
     *reinterpret_cast<uint2*>(ro + j) = make_uint2(p01, p23);
     const float b0 = bf16_lo(p01), b1 = bf16_hi(p01), b2 = bf16_lo(p23), b3 = bf16_hi(p23);
@@ -93,12 +114,13 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads)
   for (int r = 0; r < kCluster; ++r) total += *cluster.map_shared_rank(&s_part, r);
   cluster.sync();  // no CTA leaves while another still reads its s_part
   const float inv = 1.f / sqrtf(total / (float)a.H + a.eps);
-  const uint16_t* gain = reinterpret_cast<const uint16_t*>(a.gain) + c0;
   uint16_t* out = reinterpret_cast<uint16_t*>(a.out) + rowo;
-  for (int j = tid * 4; j < ncol; j += kThreads * 4) {
-    const uint2 gv = *reinterpret_cast<const uint2*>(gain + j);
-    const uint32_t p01 = pack_bf16(s_rb[j] * inv * bf16_lo(gv.x), s_rb[j + 1] * inv * bf16_hi(gv.x));
-    const uint32_t p23 = pack_bf16(s_rb[j + 2] * inv * bf16_lo(gv.y), s_rb[j + 3] * inv * bf16_hi(gv.y));
+#pragma unroll
+  for (int i = 0; i < kIter; ++i) {
+    const int j = tid * 4 + i * kThreads * 4;
+    if (j >= ncol) break;
+    const uint32_t p01 = pack_bf16(s_rb[j] * inv * bf16_lo(gv[i].x), s_rb[j + 1] * inv * bf16_hi(gv[i].x));
+    const uint32_t p23 = pack_bf16(s_rb[j + 2] * inv * bf16_lo(gv[i].y), s_rb[j + 3] * inv * bf16_hi(gv[i].y));
     *reinterpret_cast<uint2*>(out + j) = make_uint2(p01, p23);
   }
 }
