@@ -362,6 +362,19 @@ def run_ours(args, world, rank, local):
     dev = torch.device("cuda", local)
     dims = DSV3.with_(num_experts=args.num_experts)
     MS = tuple(args.ms)
+    if args.dense:
+        # profiling aid: the dense layer alone (as in the `extra` measurement)
+        fl = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+        def flush_dense():
+            fl.zero_()
+            fl.view(torch.int64).max()
+
+        res = dense_layer(m, flush_dense, dev, MS, reps=max(1, args.steps))
+        if rank == 0:
+            print(json.dumps({"metric": "dense FP8 MLP layer (DeepSeek-V3 7168 x 18432) with its boundary, us",
+                              "unit": "us", "steps": max(1, args.steps), "per_m": res}), flush=True)
+        return 0
     lw = synth.make_layer(dims, seed=0, device=dev)
     layer = m.MoeDecodeLayer(dims, lw, max_tokens=max(MS), device=dev)
     inputs = {M: synth.make_tokens(M, dims.hidden, seed=100 + M, device=dev) for M in MS}
@@ -557,6 +570,7 @@ def main():
     # profiling aids (smaller resident layer for multi-pass ncu captures)
     ap.add_argument("--num-experts", type=int, default=DSV3.num_experts)
     ap.add_argument("--ms", type=int, nargs="+", default=list(MS))
+    ap.add_argument("--dense", action="store_true", help="time only the dense layer at --ms (one untimed call first)")
     args = ap.parse_args()
     world, rank, local = dist_setup()
     if args.impl == "reference":
