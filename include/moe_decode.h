@@ -105,7 +105,7 @@ typedef struct moe_layer_weights {
 } moe_layer_weights;
 
 /* Bytes of device workspace moe_decode_layer needs for up to max_tokens
- * tokens (1 <= max_tokens, max_tokens * top_k <= 4096). */
+ * tokens (1 <= max_tokens <= 4096, max_tokens * top_k <= 4096). */
 int moe_decode_workspace_size(const moe_layer_dims *dims, int max_tokens, size_t *bytes);
 
 /* Zero a workspace (moe_decode_layer's or splitk_gemm_bf16's) once before its

@@ -119,7 +119,7 @@ int moe_decode_workspace_size(const moe_layer_dims* dims, int max_tokens, size_t
   const int rc = check_dims(dims);
   if (rc != MOE_OK) return rc;
   if (!bytes || max_tokens < 1) return MOE_ERR_INVALID_ARG;
-  if ((long long)max_tokens * dims->top_k > kMaxMk) return MOE_ERR_UNSUPPORTED;
+  if (max_tokens > kMaxTokens || (long long)max_tokens * dims->top_k > kMaxMk) return MOE_ERR_UNSUPPORTED;
   Layout L;
   layout_for(*dims, max_tokens, L);
   *bytes = L.total;
@@ -139,7 +139,7 @@ static int layer_impl(const moe_layer_dims* dims, const moe_layer_weights* w, in
   if (rc != MOE_OK) return rc;
   if (!w || M < 0) return MOE_ERR_INVALID_ARG;
   if (M == 0) return MOE_OK;
-  if ((long long)M * dims->top_k > kMaxMk) return MOE_ERR_UNSUPPORTED;
+  if (M > kMaxTokens || (long long)M * dims->top_k > kMaxMk) return MOE_ERR_UNSUPPORTED;
   const bool has_shared = dims->shared_inter > 0;
   const bool dense = dims->num_experts == 0;  // routed weights are not read (may be NULL)
   if (!dense && (!w->router_w || !w->w13 || !w->w13_s || !w->w2 || !w->w2_s)) return MOE_ERR_INVALID_ARG;

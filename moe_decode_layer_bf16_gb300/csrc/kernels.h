@@ -24,6 +24,7 @@ enum HdrWord {
 };
 constexpr int kMaxRouterTickets = 1024;
 constexpr int kMaxMk = 4096;       // M * top_k per call
+constexpr int kMaxTokens = 4096;   // M per call (the bound for a dense layer, whose top_k is 0)
 constexpr int kMaxExperts = 512;
 constexpr int kMaxTopK = 16;
 

@@ -84,6 +84,12 @@ def test_too_many_tokens_unsupported(L):
     with pytest.raises(m.MoeError) as e:
         m.moe_decode_workspace_size(DSV3, 1024)
     assert e.value.status == m.MOE_ERR_UNSUPPORTED
+    # a dense layer (top_k = 0) is bounded by the token count itself
+    from moe_decode_layer_bf16_gb300.dims import DSV3_DENSE
+    assert m.moe_decode_workspace_size(DSV3_DENSE, 4096) > 0
+    with pytest.raises(m.MoeError) as e:
+        m.moe_decode_workspace_size(DSV3_DENSE, 4097)
+    assert e.value.status == m.MOE_ERR_UNSUPPORTED
 
 
 def _weights(ptr=0x1000):
