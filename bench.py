@@ -12,7 +12,13 @@ Prints one JSON line: tokens/s over all layer calls (device time, CUDA
 events), the per-M microseconds per layer and HBM GB/s, the roofline of the
 expert kernel (algorithmic bytes / its measured duration vs the measured HBM
 copy bandwidth), the end-to-end figure through the public API with host
-buffers, the CPU oracle as a reported baseline, clocks and launch counts.
+buffers, the CPU oracle as a reported baseline (one core, and replicas on all
+cores), clocks sampled during the timed region, and launch counts.  `extra`
+times the other workloads the same way: the same layer at verify batch sizes
+(M = 64, 128, 256), the layer with skewed routing and e8m0 scales (M = 1, 16,
+128), the split-K eh_proj and the router GEMV alone at M = 1, 2, 4, 8, 16,
+the MTP front, the LM head, the dense layer and a CUDA-graph decode chain,
+with the oracle's time on one token of each workload beside them.
 
 --impl reference times the CPU oracle alone, on the same workload (a bounded
 sample per step), and prints the same kind of line with "impl": "reference".
@@ -27,12 +33,15 @@ for _v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
 import argparse
+import ctypes
 import hashlib
-import re
 import json
+import re
 import statistics
 import subprocess
 import sys
+import tempfile
+import threading
 import time
 
 import numpy as np
@@ -85,22 +94,80 @@ def load_peaks():
 
 
 class Clocks:
-    """nvidia-smi samples of the SM clock and throttle reasons while running."""
+    """The SM clock and the clock-event (throttle) reasons of the GPU, sampled
+    every 10 ms from a thread while the timed region runs (NVML through ctypes:
+    a timed region of a few tens of milliseconds still gets samples), or every
+    200 ms by nvidia-smi where NVML cannot be loaded.  Reads only."""
 
+    # NVML clock-event reason bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
     FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap,utilization.gpu")
 
-    def __init__(self, index: int):
-        self.proc = None
+    def __init__(self, local: int):
+        self.samples, self.max_mhz, self.proc, self.thread = [], None, None, None
+        self.stop_evt = threading.Event()
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._start_nvml(local)
         except Exception:
-            self.proc = None
+            self.thread = None
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self._nvml_index(local)), f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits", "-lms", "200"],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except Exception:
+                self.proc = None
+
+    @staticmethod
+    def _nvml_index(local: int) -> int:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+        if local < len(vis) and vis[local].strip().isdigit():
+            return int(vis[local])
+        return local
+
+    def _start_nvml(self, local: int):
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit")
+        h = ctypes.c_void_p()
+        ok = False
+        try:
+            u = str(torch.cuda.get_device_properties(local).uuid)
+            u = u if u.startswith("GPU-") else "GPU-" + u
+            ok = nv.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) == 0
+        except Exception:
+            ok = False
+        if not ok and nv.nvmlDeviceGetHandleByIndex_v2(self._nvml_index(local), ctypes.byref(h)) != 0:
+            raise OSError("nvml handle")
+        reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # 1 = NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+
+        def run():
+            clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+            while not self.stop_evt.is_set():
+                if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
+                        reasons_fn(h, ctypes.byref(rs)) == 0:
+                    self.samples.append((float(clk.value), int(rs.value)))
+                time.sleep(0.01)
+
+        self.thread = threading.Thread(target=run, daemon=True)
+        self.thread.start()
 
     def stop(self):
+        if self.thread is not None:
+            self.stop_evt.set()
+            self.thread.join(timeout=5)
+            if not self.samples:
+                return None
+            reasons = sorted({n for _, r in self.samples for b, n in self.REASONS.items() if r & b})
+            return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                    "reasons": reasons, "samples": len(self.samples), "source": "nvml, 10 ms"}
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -128,7 +195,7 @@ class Clocks:
         if not mx:
             return None
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(mx)}
+                "reasons": sorted(reasons), "samples": len(mx), "source": "nvidia-smi, 200 ms"}
 
 
 def dist_setup():
@@ -158,33 +225,115 @@ def max_over_ranks(v: float, world: int) -> float:
 
 # ------------------------------------------------------------------ CPU oracle
 
-def oracle_sample(seed: int = 0):
-    """One M=1 layer of the same shape, on the CPU oracle: the routing picks
-    the experts, only those are drawn.  Returns (seconds, description)."""
+def _np(t):
+    if t is None:
+        return None
+    t = t.detach().cpu()
+    return t.float().numpy().astype(np.float64) if t.dtype == torch.bfloat16 else t.numpy()
+
+
+def oracle_layer_sample(seed: int = 0, skewed: bool = False):
+    """The oracle's inputs for one token of the DeepSeek-V3-shaped layer: the
+    token, the router (and, skewed, the selection bias and Zipf popularity
+    with e8m0 scales), the shared expert, the gain and only the routed experts
+    the token is routed to (drawn seeded per expert; on the GPU when there is
+    one, which only draws random numbers).  Returns (dims, arrays dict)."""
     from oracle import moe_oracle as orc
 
-    dims = DSV3
-    x, res = synth.make_tokens(1, dims.hidden, seed=seed)
-    lw = synth.make_layer(dims, seed=seed, experts=[])  # router, shared expert, gain
+    dims = DSV3.with_(e8m0=skewed)
+    gen_dev = "cuda" if torch.cuda.is_available() else "cpu"
+    kw = dict(bias_std=0.5, zipf_s=1.1) if skewed else {}
+    x, res = synth.make_tokens(1, dims.hidden, seed=seed, device=gen_dev, zipf=skewed)
+    lw = synth.make_layer(dims, seed=seed, experts=[], device=gen_dev, **kw)
+    a = {n: _np(lw[n]) for n in ("router_w", "sel_bias", "sw13", "sw13_s", "sw2", "sw2_s", "gain")}
+    a["x"], a["res"] = _np(x), _np(res)
+    _, _, _, ids, _ = orc.route(a["x"], a["router_w"], a["sel_bias"], dims.top_k, dims.routed_scaling)
+    a["experts"] = np.asarray(sorted(set(ids.reshape(-1).tolist())), np.int64)
+    for e in a["experts"]:
+        for n, t in zip(("w13", "w13_s", "w2", "w2_s"), synth.make_expert(dims, int(e), seed=seed, device=gen_dev)):
+            a[f"{n}_{e}"] = _np(t)
+    return dims, a
 
-    def np_(t):
-        return None if t is None else (t.float().numpy().astype(np.float64) if t.dtype == torch.bfloat16
-                                       else t.numpy())
 
-    x64 = x.float().numpy().astype(np.float64)
-    _, _, _, ids, _ = orc.route(x64, np_(lw["router_w"]), None, dims.top_k, dims.routed_scaling)
-    w13, w13_s, w2, w2_s = {}, {}, {}, {}
-    for e in sorted(set(ids.reshape(-1).tolist())):
-        a, b, c, d = synth.make_expert(dims, e, seed=seed)
-        w13[e], w13_s[e], w2[e], w2_s[e] = a.numpy(), b.numpy(), c.numpy(), d.numpy()
-    L = orc.Layer(router_w=np_(lw["router_w"]), sel_bias=None, w13=w13, w13_s=w13_s, w2=w2, w2_s=w2_s,
-                  sw13=np_(lw["sw13"]), sw13_s=np_(lw["sw13_s"]), sw2=np_(lw["sw2"]), sw2_s=np_(lw["sw2_s"]),
-                  gain=np_(lw["gain"]), top_k=dims.top_k, routed_scaling=dims.routed_scaling,
-                  swiglu_limit=dims.swiglu_limit, rms_eps=dims.rms_eps, e8m0=dims.e8m0)
+def oracle_run(dims, a):
+    """The oracle's M = 1 layer call on the arrays of oracle_layer_sample:
+    seconds of the call alone."""
+    from oracle import moe_oracle as orc
+
+    ex = [int(e) for e in a["experts"]]
+    L = orc.Layer(router_w=a["router_w"], sel_bias=a.get("sel_bias"),
+                  w13={e: a[f"w13_{e}"] for e in ex}, w13_s={e: a[f"w13_s_{e}"] for e in ex},
+                  w2={e: a[f"w2_{e}"] for e in ex}, w2_s={e: a[f"w2_s_{e}"] for e in ex},
+                  sw13=a["sw13"], sw13_s=a["sw13_s"], sw2=a["sw2"], sw2_s=a["sw2_s"], gain=a["gain"],
+                  top_k=dims.top_k, routed_scaling=dims.routed_scaling, swiglu_limit=dims.swiglu_limit,
+                  rms_eps=dims.rms_eps, e8m0=dims.e8m0)
     t0 = time.perf_counter()
-    orc.moe_decode_layer(L, x64, np_(res))
-    dt = time.perf_counter() - t0
-    return dt, "one M=1 layer call (router, 8 routed + shared expert dequantised and applied, boundary)"
+    orc.moe_decode_layer(L, a["x"], a["res"])
+    return time.perf_counter() - t0
+
+
+SAMPLE_DESC = "one M=1 layer call (router, 8 routed + shared expert dequantised and applied, boundary)"
+
+
+def oracle_sample(seed: int = 0, skewed: bool = False):
+    """One M=1 layer of the same shape on the CPU oracle.  Returns (seconds,
+    description)."""
+    dims, a = oracle_layer_sample(seed, skewed)
+    return oracle_run(dims, a), SAMPLE_DESC
+
+
+def _oracle_replica(path, barrier, out):
+    # one process of the all-cores baseline: load the sample, wait for the
+    # others, time the oracle call
+    with np.load(path, allow_pickle=False) as z:
+        a = {k: z[k] for k in z.files}
+    barrier.wait()
+    dt = oracle_run(DSV3, a)
+    out.put(dt)
+
+
+def oracle_all_cores(seed: int = 0):
+    """The oracle as it stands, one replica per host core (spawned processes,
+    each single-threaded), all on the same M = 1 sample, started together:
+    tokens/s = replicas / the slowest replica's time."""
+    import multiprocessing as mp
+
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+    dims, a = oracle_layer_sample(seed)
+    with tempfile.TemporaryDirectory(dir="/dev/shm" if os.path.isdir("/dev/shm") else None) as d:
+        path = os.path.join(d, "sample.npz")
+        np.savez(path, **{k: v for k, v in a.items() if v is not None})
+        ctx = mp.get_context("spawn")
+        bar, q = ctx.Barrier(cores), ctx.Queue()
+        procs = [ctx.Process(target=_oracle_replica, args=(path, bar, q)) for _ in range(cores)]
+        for p in procs:
+            p.start()
+        dts = [q.get(timeout=600) for _ in range(cores)]
+        for p in procs:
+            p.join(timeout=60)
+    return {"value": cores / max(dts), "unit": UNIT, "cores": cores, "kind": "oracle replicas",
+            "sample": f"{cores} concurrent single-threaded replicas of the oracle, each on {SAMPLE_DESC}; "
+                      f"slowest {max(dts):.2f} s, fastest {min(dts):.2f} s"}
+
+
+def oracle_per_config(seed: int = 0):
+    """The oracle on one token of each workload the bench times (one core)."""
+    from oracle import moe_oracle as orc
+
+    res = {}
+    for name, skewed in (("deepseek_v3_uniform", False), ("deepseek_v3_skewed_e8m0", True)):
+        dt, _ = oracle_sample(seed, skewed)
+        res[name] = {"seconds": round(dt, 3), "tokens_per_s": round(1.0 / dt, 4), "sample": SAMPLE_DESC}
+    for name, (N, K) in (("splitk_eh_proj", (7168, 14336)), ("router_gemv_fp32", (256, 7168))):
+        a, w = synth.make_projection(1, N, K, seed=1,
+                                     device="cuda" if torch.cuda.is_available() else "cpu")
+        a, w = _np(a), _np(w)
+        t0 = time.perf_counter()
+        orc.projection(a, w, out_fp32=name.startswith("router"))
+        dt = time.perf_counter() - t0
+        res[name] = {"seconds": round(dt, 4), "tokens_per_s": round(1.0 / dt, 2),
+                     "sample": f"M=1 projection [1,{K}] x [{N},{K}]^T"}
+    return res
 
 
 def run_reference(args, world, rank):
@@ -210,7 +359,23 @@ def run_reference(args, world, rank):
 
 # ------------------------------------------------------------------ GPU arm
 
-def splitk_proj(m, flush_l2, dev, N, K, Ms=(1, 4, 16), reps=5):
+def timed(fn, flush_l2, reps, warm=1):
+    """Device milliseconds of fn() per call (CUDA events on the current stream,
+    L2 flushed before each call; the first `warm` calls untimed)."""
+    times = []
+    for i in range(warm + reps):
+        flush_l2()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        if i >= warm:
+            times.append(e0.elapsed_time(e1))
+    return times
+
+
+def splitk_proj(m, flush_l2, dev, N, K, Ms=(1, 2, 4, 8, 16), reps=5, fp32=False, peak=None):
     """The split-K BF16 projection Y[M, N] = A[M, K] W[N, K]^T, L2 flushed
     before every call: us and GB/s (weights + activations in + out)."""
     res = {}
@@ -218,22 +383,48 @@ def splitk_proj(m, flush_l2, dev, N, K, Ms=(1, 4, 16), reps=5):
     for M in Ms:
         a, w_m = synth.make_projection(M, N, K, seed=M, device=dev)
         w = w_m if w is None else w
-        c = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+        c = torch.empty((M, N), dtype=torch.float32 if fp32 else torch.bfloat16, device=dev)
         ws = torch.zeros(m.splitk_gemm_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
-        m.splitk_gemm_bf16(a, w, c, ws)
-        times = []
+        us = 1e3 * statistics.median(timed(lambda: m.splitk_gemm_bf16(a, w, c, ws), flush_l2, reps))
+        nbytes = 2 * N * K + 2 * M * K + c.element_size() * M * N
+        res[str(M)] = {"us": round(us, 2), "gbps": round(nbytes / us / 1e3, 1)}
+        if peak:
+            res[str(M)]["frac_of_measured"] = round(nbytes / us / 1e3 / peak, 3)
+    del w
+    torch.cuda.empty_cache()
+    return res
+
+
+def layer_block(m, dims, lw, Ms, flush_l2, dev, peak, reps=5, zipf=False, seed=500):
+    """One layer's calls at each M (L2 flushed before every call): the plain
+    call's us, tokens/s and GB/s of the layer's algorithmic bytes, and the
+    expert kernel's us from a traced call (events between the kernels)."""
+    lay = m.MoeDecodeLayer(dims, lw, max_tokens=max(Ms), device=dev)
+    res = {}
+    for M in Ms:
+        x, r = synth.make_tokens(M, dims.hidden, seed=seed + M, device=dev, zipf=zipf)
+        o, ro = torch.empty_like(x), torch.empty_like(r)
+        ids = torch.empty((M, dims.top_k), dtype=torch.int32, device=dev)
+        plain = timed(lambda: lay(x, r, o, ro, topk_ids=ids), flush_l2, reps)
+        exp_ms = []
         for _ in range(reps):
             flush_l2()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            m.splitk_gemm_bf16(a, w, c, ws)
-            e1.record()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            m.moe_decode_layer_traced(dims, lw, x, r, o, ro, lay.workspace, ev, topk_ids=ids)
             torch.cuda.synchronize()
-            times.append(e0.elapsed_time(e1))
-        us = 1e3 * statistics.median(times)
-        nbytes = 2 * N * K + 2 * M * K + 2 * M * N
-        res[str(M)] = {"us": round(us, 2), "gbps": round(nbytes / us / 1e3, 1)}
-    del w
+            exp_ms.append(ev[1].elapsed_time(ev[2]))
+        if lay.status() != m.MOE_OK:
+            raise RuntimeError("layer status")
+        unique = int(torch.unique(ids).numel())
+        us, ue = 1e3 * statistics.median(plain), 1e3 * statistics.median(exp_ms)
+        lb = layer_bytes(M, unique)
+        res[str(M)] = {"us_per_layer": round(us, 2), "tokens_per_s": round(M * 1e6 / us, 1),
+                       "unique_experts": unique, "layer_gbps": round(lb / us / 1e3, 1),
+                       "frac_of_8TBs": round(lb / us / 1e3 / 8000.0, 3),
+                       "frac_of_measured": round(lb / us / 1e3 / peak, 3),
+                       "us_experts": round(ue, 2),
+                       "experts_frac_of_measured": round((unique + 1) * EXPERT_BYTES / ue / 1e3 / peak, 3)}
+    del lay
     torch.cuda.empty_cache()
     return res
 
@@ -495,42 +686,60 @@ def run_ours(args, world, rank, local):
 
     extra = {}
     if not args.no_extras:
-        try:
-            extra["graph_chain"] = {
-                "what": "3 layers with distinct weights captured as one CUDA graph, each layer's outputs "
-                        "feeding the next, replayed back to back without L2 flushes",
-                "per_m": graph_chain(m, dims, lw, MS, 3, 10, dev)}
-        except Exception as exc:  # reported, not fatal: the headline does not depend on it
-            extra["graph_chain"] = {"error": f"{type(exc).__name__}: {exc}"}
-        try:
-            extra["splitk_eh_proj"] = {"what": "splitk_gemm_bf16, MTP eh_proj N=7168 K=14336 (205.5 MB), "
-                                               "L2 flushed, median of 5",
-                                       "per_m": splitk_proj(m, flush_l2, dev, 7168, 14336)}
-        except Exception as exc:
-            extra["splitk_eh_proj"] = {"error": f"{type(exc).__name__}: {exc}"}
-        try:
-            extra["dense_layer"] = {"what": "DeepSeek-V3 dense layer (FP8 MLP 7168 x 18432, 396 MB) with its "
-                                            "boundary, L2 flushed, median of 5",
-                                    "per_m": dense_layer(m, flush_l2, dev, MS)}
-        except Exception as exc:
-            extra["dense_layer"] = {"error": f"{type(exc).__name__}: {exc}"}
-        try:
-            extra["mtp_eh_front"] = {"what": "mtp_eh_front, H=7168, vocab 129280, eh_proj [7168, 14336] (205.5 MB), "
-                                             "L2 flushed, median of 5",
-                                     "per_m": mtp_front(m, flush_l2, dev)}
-        except Exception as exc:
-            extra["mtp_eh_front"] = {"error": f"{type(exc).__name__}: {exc}"}
-        try:
-            extra["splitk_lm_head"] = {"what": "splitk_gemm_bf16, LM head N=129280 K=7168 (1.85 GB), "
-                                               "L2 flushed, median of 5",
-                                       "per_m": splitk_proj(m, flush_l2, dev, 129280, 7168, Ms=(1, 8))}
-        except Exception as exc:
-            extra["splitk_lm_head"] = {"error": f"{type(exc).__name__}: {exc}"}
+        def attempt(key, what, fn):
+            # reported, not fatal: the headline does not depend on the extras
+            try:
+                extra[key] = {"what": what, "per_m": fn()}
+            except Exception as exc:
+                extra[key] = {"what": what, "error": f"{type(exc).__name__}: {exc}"}
+
+        attempt("verify_batches", "the same layer at verify / grouped batch sizes M = 64, 128, 256 (i.i.d. router "
+                "logits: nearly every expert active), L2 flushed, median of 5; us_experts from a traced call",
+                lambda: layer_block(m, dims, lw, (64, 128, 256), flush_l2, dev, peak))
+        if dims.num_experts == DSV3.num_experts:
+            def skewed():
+                d4 = DSV3.with_(e8m0=True)
+                lw4 = synth.make_layer(d4, seed=4, device=dev, bias_std=0.5, zipf_s=1.1)
+                try:
+                    return layer_block(m, d4, lw4, (1, 16, 128), flush_l2, dev, peak, zipf=True, seed=600)
+                finally:
+                    del lw4
+                    torch.cuda.empty_cache()
+
+            attempt("skewed_e8m0", "the DeepSeek-V3-shaped layer with power-of-two (e8m0) scales, a selection bias "
+                    "~N(0,0.5) and Zipf(1.1) expert popularity, M = 1, 16, 128, L2 flushed, median of 5",
+                    skewed)
+        attempt("splitk_eh_proj", "splitk_gemm_bf16 (split_k = 0: stream-K), MTP eh_proj N=7168 K=14336 "
+                "(205.5 MB), L2 flushed, median of 5",
+                lambda: splitk_proj(m, flush_l2, dev, 7168, 14336, peak=peak))
+        attempt("router_gemv", "the router GEMV alone as the split-K projection's fp32 form, "
+                "[M,7168] x [256,7168]^T -> fp32 logits (3.67 MB: launch-bound, its fraction of the HBM "
+                "roofline is not meaningful), L2 flushed, median of 5",
+                lambda: splitk_proj(m, flush_l2, dev, 256, 7168, fp32=True))
+        attempt("graph_chain", "3 layers with distinct weights captured as one CUDA graph, each layer's outputs "
+                "feeding the next, replayed back to back without L2 flushes",
+                lambda: graph_chain(m, dims, lw, MS, 3, 10, dev))
+        attempt("dense_layer", "DeepSeek-V3 dense layer (FP8 MLP 7168 x 18432, 396 MB) with its boundary, "
+                "L2 flushed, median of 5", lambda: dense_layer(m, flush_l2, dev, MS))
+        attempt("mtp_eh_front", "mtp_eh_front, H=7168, vocab 129280, eh_proj [7168, 14336] (205.5 MB), "
+                "L2 flushed, median of 5", lambda: mtp_front(m, flush_l2, dev))
+        attempt("splitk_lm_head", "splitk_gemm_bf16, LM head N=129280 K=7168 (1.85 GB), L2 flushed, median of 5",
+                lambda: splitk_proj(m, flush_l2, dev, 129280, 7168, Ms=(1, 8), peak=peak))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         dt, desc = oracle_sample(seed=0)
         cpu = {"value": 1.0 / dt, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": desc}
+        try:
+            cpu["all_cores"] = oracle_all_cores(seed=0)
+        except Exception as exc:
+            cpu["all_cores"] = {"error": f"{type(exc).__name__}: {exc}"}
+        if not args.no_extras:
+            try:
+                extra["oracle_per_config"] = {"what": "the oracle (one core) on one token of each workload",
+                                              "per_config": oracle_per_config(seed=0)}
+            except Exception as exc:
+                extra["oracle_per_config"] = {"error": f"{type(exc).__name__}: {exc}"}
 
     workload = WORKLOAD if (dims.num_experts == DSV3.num_experts and MS == (1, 8, 32)) else (
         f"profiling case: H=7168 E={dims.num_experts} k=8 I=Is=2048, M in {set(MS)}")
@@ -566,7 +775,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--no-extras", action="store_true", help="skip the graph-chain and split-K measurements")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the other workloads (verify batches, skewed routing, split-K, router, graph chain, "
+                         "dense layer, MTP front, LM head)")
     # profiling aids (smaller resident layer for multi-pass ncu captures)
     ap.add_argument("--num-experts", type=int, default=DSV3.num_experts)
     ap.add_argument("--ms", type=int, nargs="+", default=list(MS))

@@ -165,21 +165,28 @@ int moe_decode_layer_traced(const moe_layer_dims *dims, const moe_layer_weights 
                             int32_t *expert_offsets, void *workspace, size_t ws_bytes,
                             void *stream, void *const *events);
 
-/* Bytes of workspace splitk_gemm_bf16 needs for this shape. */
-int splitk_gemm_workspace_size(int M, int N, int K, size_t *bytes);
+/* Bytes of workspace splitk_gemm_bf16 needs for this shape and split_k. */
+int splitk_gemm_workspace_size(int M, int N, int K, int split_k, size_t *bytes);
 
 /*
  * Split-K BF16 projection ([draft page] module docstring: the draft's BF16
  * projections such as eh_proj run a split-K GEMM above two tokens;
- * SpecializedDraft.run):
+ * SpecializedDraft.run.  [decode page] LayerStages._router passes its split
+ * count to the router's split-K GEMM explicitly):
  *   C[M, N] = alpha * A[M, K] . W[N, K]^T, fp32 accumulation.
  *   A bf16 [M, K]; W bf16 [N, K]; C bf16 [M, N] (c_fp32 == 0) or fp32 [M, N].
  *   1 <= M <= 256, N % 16 == 0, K % 128 == 0; A, W 16-byte aligned.
- * The K dimension is divided over the whole GPU (stream-K); partial sums are
- * reduced in a fixed order, so results are deterministic.
+ *   split_k  0: the library divides the K dimension over the whole GPU
+ *            (stream-K: every SM streams an equal share of W);
+ *            S > 0: every (token chunk, 64-row tile) of C is cut into exactly
+ *            S K-segments of K/(128 S) k-blocks each (rounded), one CTA a
+ *            segment; 1 <= S <= K/128 (MOE_ERR_UNSUPPORTED above, a negative
+ *            value is MOE_ERR_INVALID_ARG).
+ * Partial sums are reduced in segment order, so results are deterministic for
+ * a given split; different splits may differ in the last bits.
  */
 int splitk_gemm_bf16(const void *A, const void *W, void *C, int c_fp32, int M, int N, int K,
-                     float alpha, void *ws, size_t ws_bytes, void *stream);
+                     int split_k, float alpha, void *ws, size_t ws_bytes, void *stream);
 
 /*
  * splitk_gemm_bf16 without a caller-provided workspace, for callers that
@@ -188,7 +195,8 @@ int splitk_gemm_bf16(const void *A, const void *W, void *C, int c_fp32, int M, i
  * runtime that hands out only a fixed pool it owns).  No counterpart on the
  * source pages: this is an interface convenience of this library.
  *
- * Same arguments and result as splitk_gemm_bf16, minus ws / ws_bytes.  The
+ * Same arguments and result as splitk_gemm_bf16 (the same plan, hence the
+ * same bits), minus ws / ws_bytes.  The
  * partial sums and tile counters live in one static device array of
  * MOE_NOALLOC_SCRATCH_BYTES (8 MiB) in the library, which every GPU that
  * loads the library holds until the process exits.  Nothing is allocated or
@@ -203,7 +211,12 @@ int splitk_gemm_bf16(const void *A, const void *W, void *C, int c_fp32, int M, i
  */
 #define MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
 int splitk_gemm_bf16_noalloc(const void *A, const void *W, void *C, int c_fp32, int M, int N, int K,
-                             float alpha, void *stream);
+                             int split_k, float alpha, void *stream);
+
+/* Test hook: fill the whole static scratch of splitk_gemm_bf16_noalloc on the
+ * current device with `byte` (stream-ordered), so that a test can check that
+ * a call clears the counters it uses whatever an earlier call left there. */
+int moe_debug_fill_noalloc_scratch(int byte, void *stream);
 
 /*
  * Layer boundary: optional weighted top-k finalize, residual add, RMSNorm

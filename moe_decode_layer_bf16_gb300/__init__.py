@@ -71,9 +71,10 @@ def lib() -> ctypes.CDLL:
         L.moe_decode_layer.argtypes = [ctypes.POINTER(_Dims), ctypes.POINTER(_Weights), _i, _vp, _vp, _vp,
                                        _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
         L.moe_decode_layer_traced.argtypes = L.moe_decode_layer.argtypes + [ctypes.POINTER(_vp)]
-        L.splitk_gemm_workspace_size.argtypes = [_i, _i, _i, ctypes.POINTER(_sz)]
-        L.splitk_gemm_bf16.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _f, _vp, _sz, _vp]
-        L.splitk_gemm_bf16_noalloc.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _f, _vp]
+        L.splitk_gemm_workspace_size.argtypes = [_i, _i, _i, _i, ctypes.POINTER(_sz)]
+        L.splitk_gemm_bf16.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]
+        L.splitk_gemm_bf16_noalloc.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]
+        L.moe_debug_fill_noalloc_scratch.argtypes = [_i, _vp]
         L.rmsnorm_residual.argtypes = [_vp, _vp, _vp, _i, _i, _f, _vp, _vp, _i, _vp, _vp, _vp, _vp]
         L.mtp_eh_front_workspace_size.argtypes = [_i, _i, ctypes.POINTER(_sz)]
         L.mtp_eh_front.argtypes = [_vp, _vp, _i, _vp, _vp, _vp, _f, _vp, _i, _i, _vp, _vp, _sz, _vp]
@@ -83,7 +84,8 @@ def lib() -> ctypes.CDLL:
         L.moe_status_str.restype = ctypes.c_char_p
         for n in ("moe_decode_workspace_size", "moe_workspace_init", "moe_decode_layer", "moe_decode_layer_traced",
                   "splitk_gemm_workspace_size", "splitk_gemm_bf16", "splitk_gemm_bf16_noalloc", "rmsnorm_residual",
-                  "moe_device_status", "moe_debug_set_fault", "mtp_eh_front_workspace_size", "mtp_eh_front"):
+                  "moe_device_status", "moe_debug_set_fault", "moe_debug_fill_noalloc_scratch",
+                  "mtp_eh_front_workspace_size", "mtp_eh_front"):
             getattr(L, n).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -167,25 +169,27 @@ def moe_decode_layer_traced(dims: LayerDims, weights: dict, x, residual, out, re
     _check(rc, "moe_decode_layer_traced")
 
 
-def splitk_gemm_workspace_size(M: int, N: int, K: int) -> int:
+def splitk_gemm_workspace_size(M: int, N: int, K: int, split_k: int = 0) -> int:
     n = _sz(0)
-    _check(lib().splitk_gemm_workspace_size(int(M), int(N), int(K), ctypes.byref(n)),
+    _check(lib().splitk_gemm_workspace_size(int(M), int(N), int(K), int(split_k), ctypes.byref(n)),
            "splitk_gemm_workspace_size")
     return n.value
 
 
-def splitk_gemm_bf16(A, W, C, workspace, alpha: float = 1.0, stream=None):
-    """C = alpha * A . W^T; C's dtype (bf16 or float32) selects the output form."""
+def splitk_gemm_bf16(A, W, C, workspace, alpha: float = 1.0, split_k: int = 0, stream=None):
+    """C = alpha * A . W^T; C's dtype (bf16 or float32) selects the output form.
+    split_k = 0 lets the library divide K over the whole GPU; S > 0 cuts every
+    64-row tile into S K-segments (the workspace must be sized for that S)."""
     import torch
     M, K = A.shape
     N = W.shape[0]
     rc = lib().splitk_gemm_bf16(_ptr(A), _ptr(W), _ptr(C), 1 if C.dtype == torch.float32 else 0, M, N, K,
-                                float(alpha), _ptr(workspace), workspace.numel() * workspace.element_size(),
-                                _stream(stream))
+                                int(split_k), float(alpha), _ptr(workspace),
+                                workspace.numel() * workspace.element_size(), _stream(stream))
     _check(rc, "splitk_gemm_bf16")
 
 
-def splitk_gemm_bf16_noalloc(A, W, C, alpha: float = 1.0, stream=None):
+def splitk_gemm_bf16_noalloc(A, W, C, alpha: float = 1.0, split_k: int = 0, stream=None):
     """splitk_gemm_bf16 with the library's static scratch instead of a caller
     workspace, for callers that cannot allocate device memory where they run
     the projection.  Calls that may overlap on the GPU must not share it."""
@@ -193,8 +197,13 @@ def splitk_gemm_bf16_noalloc(A, W, C, alpha: float = 1.0, stream=None):
     M, K = A.shape
     N = W.shape[0]
     rc = lib().splitk_gemm_bf16_noalloc(_ptr(A), _ptr(W), _ptr(C), 1 if C.dtype == torch.float32 else 0, M, N, K,
-                                        float(alpha), _stream(stream))
+                                        int(split_k), float(alpha), _stream(stream))
     _check(rc, "splitk_gemm_bf16_noalloc")
+
+
+def moe_debug_fill_noalloc_scratch(byte: int, stream=None):
+    """Test hook: fill the no-allocation entry point's static scratch with `byte`."""
+    _check(lib().moe_debug_fill_noalloc_scratch(int(byte), _stream(stream)), "moe_debug_fill_noalloc_scratch")
 
 
 def mtp_eh_front_workspace_size(M: int, H: int) -> int:

@@ -1,6 +1,8 @@
 // C ABI of libmoe_decode.so (declared in include/moe_decode.h): argument
 // checks, workspace layout and kernel launches.  Host code only.
 #include <algorithm>
+#include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstring>
 
@@ -21,7 +23,7 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 // CTAs: nkb contiguous cells meet at most ceil(nkb / shortest run) + 1 runs.
 size_t gemv_partials_bound(int M, int N, int K) {
   GemvPlan p;
-  p.chunk_tokens = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
+  p.chunk_tokens = gemv_chunk_tokens(M);
   p.n_chunks = (M + p.chunk_tokens - 1) / p.chunk_tokens;
   p.n_tiles = (N + 63) / 64;
   p.nkb = K / kBlock;
@@ -89,25 +91,63 @@ int check_dims(const moe_layer_dims* d) {
   return MOE_OK;
 }
 
-int sm_count_cached(int* out) {
-  static int cache[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-  if (!cache[dev]) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      return MOE_ERR_CUDA;
-    cache[dev] = n;
-  }
-  *out = cache[dev];
-  return MOE_OK;
-}
-
 int gemv_grid(long long cells, int sms, int per_sm) {
   return (int)std::max<long long>(1, std::min<long long>({cells, (long long)sms * per_sm, (long long)kGemvMaxCtas}));
 }
 
+int check_splitk_shape(int M, int N, int K, int split_k) {
+  if (M < 1 || N < 1 || K < 1 || split_k < 0) return MOE_ERR_INVALID_ARG;
+  if (M > 256 || N % 16 || K % kBlock) return MOE_ERR_UNSUPPORTED;
+  if (split_k > K / kBlock) return MOE_ERR_UNSUPPORTED;  // at most one k-block per segment
+  return MOE_OK;
+}
+
+long long tiles_of(int M, int N) {
+  const int chunk = gemv_chunk_tokens(M);
+  return (long long)((M + chunk - 1) / chunk) * ((N + 63) / 64);
+}
+
 }  // namespace
+
+// Host threads may make their first calls at the same time: the cached values
+// are atomics (a race only computes the same value twice).
+int current_device_sms(int* out) {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (!n) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return MOE_ERR_CUDA;
+    cache[dev].store(n, std::memory_order_relaxed);
+  }
+  *out = n;
+  return MOE_OK;
+}
+
+int plan_splitk(GemvPlan& plan, int M, int N, int K, int split_k) {
+  int rc = check_splitk_shape(M, N, K, split_k);
+  if (rc != MOE_OK) return rc;
+  const long long n_ct = tiles_of(M, N);
+  long long G;
+  if (split_k > 0) {
+    // CTA c owns cells [c T / G, (c + 1) T / G) with T = n_ct * nkb and
+    // G = n_ct * S: the runs start at every tile's first k-block and cut
+    // each tile into exactly S segments
+    G = n_ct * split_k;
+    if (G > INT_MAX) return MOE_ERR_UNSUPPORTED;
+  } else {
+    int sms = 0;
+    if ((rc = current_device_sms(&sms)) != MOE_OK) return rc;
+    G = gemv_grid(n_ct * (K / kBlock), sms, gemv_blocks_per_sm(gemv_chunk_tokens(M), false));
+  }
+  plan_gemv(plan, M, N, K, (int)G);
+  return MOE_OK;
+}
+
+size_t splitk_ticket_bytes(const GemvPlan& p) { return align_up((size_t)p.n_chunks * p.n_tiles * sizeof(unsigned)); }
+
+size_t splitk_partial_bytes(const GemvPlan& p) { return p.max_segs > 1 ? gemv_partials_bytes(p) : 0; }
 
 }  // namespace moe
 
@@ -154,13 +194,13 @@ static int layer_impl(const moe_layer_dims* dims, const moe_layer_weights* w, in
   layout_for(*dims, M, L);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
   int sms = 0;
-  if ((rc = sm_count_cached(&sms)) != MOE_OK) return rc;
+  if ((rc = current_device_sms(&sms)) != MOE_OK) return rc;
   cudaStream_t s = (cudaStream_t)stream;
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
   const int H = dims->hidden, E = dims->num_experts, k = dims->top_k;
 
   GemvPlan plan;
-  const int chunk = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
+  const int chunk = gemv_chunk_tokens(M);
   const long long cells = (long long)((M + chunk - 1) / chunk) * ((E + 63) / 64) * (H / kBlock);
   // at least 2 (M <= 8) or 4 k-blocks per CTA: shorter runs start the routing
   // sooner at one token chunk, more partial sums to add cost more above (measured)
@@ -251,34 +291,33 @@ int moe_decode_layer_traced(const moe_layer_dims* dims, const moe_layer_weights*
                     expert_offsets, workspace, ws_bytes, stream, events);
 }
 
-int splitk_gemm_workspace_size(int M, int N, int K, size_t* bytes) {
-  if (!bytes || M < 1 || N < 1 || K < 1) return MOE_ERR_INVALID_ARG;
-  if (M > 256 || N % 16 || K % kBlock) return MOE_ERR_UNSUPPORTED;
-  GemvPlan p;
-  p.chunk_tokens = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
-  const size_t tickets = (size_t)((M + p.chunk_tokens - 1) / p.chunk_tokens) * ((N + 63) / 64);
-  *bytes = align_up(tickets * sizeof(unsigned)) + gemv_partials_bound(M, N, K);
+int splitk_gemm_workspace_size(int M, int N, int K, int split_k, size_t* bytes) {
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  const int rc = check_splitk_shape(M, N, K, split_k);
+  if (rc != MOE_OK) return rc;
+  const long long n_ct = tiles_of(M, N);
+  // the automatic split depends on the device's SM count: its bound covers any grid
+  const size_t partials = split_k == 0 ? gemv_partials_bound(M, N, K)
+                          : split_k == 1 ? 0
+                                         : (size_t)n_ct * split_k * gemv_chunk_tokens(M) * 64 * sizeof(float);
+  *bytes = align_up((size_t)n_ct * sizeof(unsigned)) + partials;
   return MOE_OK;
 }
 
-int splitk_gemm_bf16(const void* A, const void* W, void* C, int c_fp32, int M, int N, int K, float alpha,
-                     void* ws, size_t ws_bytes, void* stream) {
+int splitk_gemm_bf16(const void* A, const void* W, void* C, int c_fp32, int M, int N, int K, int split_k,
+                     float alpha, void* ws, size_t ws_bytes, void* stream) {
   size_t need = 0;
-  int rc = splitk_gemm_workspace_size(M, N, K, &need);
+  int rc = splitk_gemm_workspace_size(M, N, K, split_k, &need);
   if (rc != MOE_OK) return rc;
   if (!A || !W || !C || !ws) return MOE_ERR_INVALID_ARG;
   if (!aligned16(A) || !aligned16(W) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
   if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  int sms = 0;
-  if ((rc = sm_count_cached(&sms)) != MOE_OK) return rc;
   GemvPlan plan;
-  const int chunk = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
-  const long long cells = (long long)((M + chunk - 1) / chunk) * ((N + 63) / 64) * (K / kBlock);
-  plan_gemv(plan, M, N, K, gemv_grid(cells, sms, gemv_blocks_per_sm(chunk, false)));
-  if (gemv_partials_bytes(plan) > gemv_partials_bound(M, N, K)) return MOE_ERR_UNSUPPORTED;
+  if ((rc = plan_splitk(plan, M, N, K, split_k)) != MOE_OK) return rc;
+  const size_t tickets = splitk_ticket_bytes(plan);
+  if (tickets + splitk_partial_bytes(plan) > need) return MOE_ERR_UNSUPPORTED;
   SplitKArgs a;
   a.A = A; a.W = W; a.C = C; a.c_fp32 = c_fp32 ? 1 : 0; a.alpha = alpha;
-  const size_t tickets = align_up((size_t)plan.n_chunks * plan.n_tiles * sizeof(unsigned));
   a.tickets = reinterpret_cast<unsigned*>(ws);
   a.partials = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + tickets);
   return launch_splitk(plan, a, (cudaStream_t)stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
@@ -311,7 +350,7 @@ int mtp_eh_front_workspace_size(int M, int H, size_t* bytes) {
   if (!bytes || M < 1 || H < 1) return MOE_ERR_INVALID_ARG;
   if (M > 256 || H % kBlock || H > 16384) return MOE_ERR_UNSUPPORTED;
   size_t gemm = 0;
-  const int rc = splitk_gemm_workspace_size(M, H, 2 * H, &gemm);
+  const int rc = splitk_gemm_workspace_size(M, H, 2 * H, 0, &gemm);
   if (rc != MOE_OK) return rc;
   *bytes = kMtpHdr + align_up((size_t)M * 2 * H * 2) + gemm;
   return MOE_OK;
@@ -337,7 +376,7 @@ int mtp_eh_front(const int32_t* input_ids, const void* embed, int vocab, const v
   ea.eps = eps; ea.out = A; ea.M = M; ea.H = H;
   ea.status = reinterpret_cast<int*>(w) + kHdrStatus;
   if (launch_eh_norm(ea, (cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
-  return splitk_gemm_bf16(A, eh_proj_w, out, 0, M, H, 2 * H, 1.f, gemm_ws, need - (gemm_ws - w), stream);
+  return splitk_gemm_bf16(A, eh_proj_w, out, 0, M, H, 2 * H, 0, 1.f, gemm_ws, need - (gemm_ws - w), stream);
 }
 
 int moe_device_status(void* ws, void* stream) {

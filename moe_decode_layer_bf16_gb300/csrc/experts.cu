@@ -144,6 +144,20 @@ MOE_DEV bool mbar_wait(uint64_t* b, uint32_t parity, int* status) {
   atomicExch(status, MOE_ERR_DEVICE_TIMEOUT);
   return false;
 }
+// Wait for copies this CTA has issued, bounded by time only: unlike mbar_wait
+// it does not give up when another wait of the grid has failed, because issued
+// copies always land and the CTA may not leave while one still writes into its
+// shared memory.  False (and the status word set) only when the bound ran out.
+MOE_DEV bool mbar_wait_landed(uint64_t* b, uint32_t parity, int* status) {
+  if (mbar_try_wait(b, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (long it = 1; it < (1l << 26); ++it) {
+    if (mbar_try_wait(b, parity)) return true;
+    if ((it & 63) == 0 && globaltimer_ns() - t0 > kWaitNs) break;
+  }
+  atomicExch(status, MOE_ERR_DEVICE_TIMEOUT);
+  return false;
+}
 MOE_DEV void tma_load_5d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3, int c4,
                          uint64_t* bar) {
   asm volatile(
@@ -535,9 +549,11 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
         ++gs;
       }
     }
+    // (every stage up to gs was armed and its copies issued in the same step;
+    // the last nst of them are the only ones whose slots were not reused)
     if (lane == 0)
       for (uint32_t j = (gs > (uint32_t)nst ? gs - nst : 0); j < gs; ++j)
-        mbar_wait(full + (j % nst), (j / nst) & 1u, status);
+        mbar_wait_landed(full + (j % nst), (j / nst) & 1u, status);
     __syncwarp();
   } else if (warp == kEW) {
     // ================================================================ epilogue

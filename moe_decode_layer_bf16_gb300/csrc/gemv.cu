@@ -15,6 +15,7 @@
 // of a tile leaves one fp32 partial, and the last CTA to finish a tile sums
 // the partials in segment order (deterministic) and applies the epilogue.
 #include <algorithm>
+#include <atomic>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -501,7 +502,7 @@ static int cta_of_cell_host(long long x, long long total, int G) {
 
 void plan_gemv(GemvPlan& p, int M, int N, int K, int G) {
   p.M = M; p.N = N; p.K = K;
-  p.chunk_tokens = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
+  p.chunk_tokens = gemv_chunk_tokens(M);
   p.n_chunks = (M + p.chunk_tokens - 1) / p.chunk_tokens;
   p.n_tiles = (N + 63) / 64;
   p.nkb = K / kBlock;
@@ -520,9 +521,13 @@ size_t gemv_partials_bytes(const GemvPlan& p) {
 }
 
 int gemv_blocks_per_sm(int chunk_tokens, bool router) {
-  static int cache[2][3] = {{0, 0, 0}, {0, 0, 0}};
+  // per device; host threads may race on a first call (both store the same value)
+  static std::atomic<int> cache[64][2][3];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
   const int i = chunk_tokens == 8 ? 0 : (chunk_tokens == 16 ? 1 : 2);
-  int& c = cache[router ? 1 : 0][i];
+  std::atomic<int>& slot = cache[dev][router ? 1 : 0][i];
+  int c = slot.load(std::memory_order_relaxed);
   if (!c) {
     int n = 0;
     cudaError_t e;
@@ -535,6 +540,7 @@ int gemv_blocks_per_sm(int chunk_tokens, bool router) {
         : i == 1 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, splitk_kernel<2>, kThreads, 0)
                  : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, splitk_kernel<4>, kThreads, 0);
     c = (e == cudaSuccess && n > 0) ? n : 1;
+    slot.store(c, std::memory_order_relaxed);
   }
   return c;
 }
@@ -575,40 +581,54 @@ cudaError_t launch_router(const GemvPlan& p, const RouterArgs& a, cudaStream_t s
 namespace {
 constexpr size_t kNoallocTicketBytes = 64 * 1024;  // up to 16384 (chunk, tile) counters
 static __device__ __align__(256) uint8_t g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+// Device address of the scratch on the current device; the lookup runs on
+// the first call per device (host threads racing on it store the same value).
+int noalloc_base(uint8_t** out) {
+  static std::atomic<uint8_t*> base[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  uint8_t* b = base[dev].load(std::memory_order_acquire);
+  if (!b) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return MOE_ERR_CUDA;
+    b = reinterpret_cast<uint8_t*>(ptr);
+    base[dev].store(b, std::memory_order_release);
+  }
+  *out = b;
+  return MOE_OK;
+}
 }  // namespace
 
 extern "C" int splitk_gemm_bf16_noalloc(const void* A, const void* W, void* C, int c_fp32, int M, int N, int K,
-                                        float alpha, void* stream) {
+                                        int split_k, float alpha, void* stream) {
   using namespace moe;
-  if (M < 1 || N < 1 || K < 1) return MOE_ERR_INVALID_ARG;
-  if (M > 256 || N % 16 || K % kBlock) return MOE_ERR_UNSUPPORTED;
+  // the same plan (grid, split, reduction order) as splitk_gemm_bf16
+  GemvPlan plan;
+  int rc = plan_splitk(plan, M, N, K, split_k);
+  if (rc != MOE_OK) return rc;
   if (!A || !W || !C) return MOE_ERR_INVALID_ARG;
   if (((uintptr_t)A & 15u) || ((uintptr_t)W & 15u)) return MOE_ERR_INVALID_ARG;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
-  static uint8_t* base[64] = {nullptr};
-  if (!base[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) return MOE_ERR_CUDA;
-    base[dev] = reinterpret_cast<uint8_t*>(ptr);
-  }
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-    return MOE_ERR_CUDA;
-  const int chunk = M <= 8 ? 8 : (M <= 16 ? 16 : 32);
-  const long long cells = (long long)((M + chunk - 1) / chunk) * ((N + 63) / 64) * (K / kBlock);
-  const int per_sm = gemv_blocks_per_sm(chunk, false);
-  GemvPlan plan;
-  plan_gemv(plan, M, N, K, (int)std::max<long long>(1, std::min<long long>({cells, (long long)sms * per_sm, 2048ll})));
-  const size_t tickets = (size_t)plan.n_chunks * plan.n_tiles * sizeof(unsigned);
-  if (tickets > kNoallocTicketBytes || kNoallocTicketBytes + gemv_partials_bytes(plan) > MOE_NOALLOC_SCRATCH_BYTES)
+  const size_t tickets = splitk_ticket_bytes(plan);
+  if (tickets > kNoallocTicketBytes || kNoallocTicketBytes + splitk_partial_bytes(plan) > MOE_NOALLOC_SCRATCH_BYTES)
     return MOE_ERR_SCRATCH_LIMIT;
+  uint8_t* base = nullptr;
+  if ((rc = noalloc_base(&base)) != MOE_OK) return rc;
   cudaStream_t s = (cudaStream_t)stream;
   // the counters must start at zero whatever an earlier call left behind
-  if (cudaMemsetAsync(base[dev], 0, tickets, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(base, 0, tickets, s) != cudaSuccess) return MOE_ERR_CUDA;
   SplitKArgs a;
   a.A = A; a.W = W; a.C = C; a.c_fp32 = c_fp32 ? 1 : 0; a.alpha = alpha;
-  a.tickets = reinterpret_cast<unsigned*>(base[dev]);
-  a.partials = reinterpret_cast<float*>(base[dev] + kNoallocTicketBytes);
+  a.tickets = reinterpret_cast<unsigned*>(base);
+  a.partials = reinterpret_cast<float*>(base + kNoallocTicketBytes);
   return launch_splitk(plan, a, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+extern "C" int moe_debug_fill_noalloc_scratch(int byte, void* stream) {
+  uint8_t* base = nullptr;
+  const int rc = noalloc_base(&base);
+  if (rc != MOE_OK) return rc;
+  return cudaMemsetAsync(base, byte & 0xff, MOE_NOALLOC_SCRATCH_BYTES, (cudaStream_t)stream) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}

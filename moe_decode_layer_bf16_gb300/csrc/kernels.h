@@ -40,9 +40,25 @@ struct GemvPlan {
   int max_segs;      // most segments that cover one (chunk, tile)
 };
 void plan_gemv(GemvPlan& p, int M, int N, int K, int G);
-// resident CTAs per SM of the split-K (router == false) or router kernel
+// resident CTAs per SM of the split-K (router == false) or router kernel on
+// the current device (cached per device)
 int gemv_blocks_per_sm(int chunk_tokens, bool router);
 size_t gemv_partials_bytes(const GemvPlan& p);
+// token chunk of a skinny GEMM of M tokens: 8, 16 or 32 columns per CTA pass
+inline int gemv_chunk_tokens(int M) { return M <= 8 ? 8 : (M <= 16 ? 16 : 32); }
+
+// SM count of the current device (cached per device): MOE_OK or MOE_ERR_CUDA.
+int current_device_sms(int* sms);
+// The plan of one split-K projection, shared by every entry point that runs
+// it.  split_k == 0: stream-K over all SMs (every CTA streams an equal share
+// of W); split_k = S > 0: every (token chunk, 64-row tile) is cut into exactly
+// S K-segments, one CTA each.  Returns MOE_OK, MOE_ERR_INVALID_ARG or
+// MOE_ERR_UNSUPPORTED (shape or split out of range) or MOE_ERR_CUDA.
+int plan_splitk(GemvPlan& p, int M, int N, int K, int split_k);
+// Bytes of the plan's tile counters (one per (chunk, tile), rounded up to
+// 256) and of its partial sums (0 when no tile is split).
+size_t splitk_ticket_bytes(const GemvPlan& p);
+size_t splitk_partial_bytes(const GemvPlan& p);
 
 struct SplitKArgs {
   const void* A;
@@ -121,8 +137,6 @@ struct EhNormArgs {
   int* status;
 };
 cudaError_t launch_eh_norm(const EhNormArgs& a, cudaStream_t s);
-
-int device_sm_count();
 
 // Launch configuration that lets a kernel start while its predecessor in the
 // stream finishes (it waits with griddepcontrol.wait before using its results).

@@ -20,8 +20,11 @@ square root).  Every reading taken where the pages are silent is listed in the
 repository's design notes and repeated at the function that takes it.
 
 Precision: float64 throughout, except where floating point decides an integer
-(an FP8 code, a top-k choice).  Those decisions are taken in float32, the
-precision the kernels take them in:
+(an FP8 code, a top-k choice).  The method is stated in fp32; float64 is read
+as "no coarser than fp32": every sum the oracle forms is at least as exact as
+an fp32 one, so the gap to the GPU path is the GPU's own rounding.  The
+integer-deciding steps are taken in float32, the precision the kernels take
+them in:
   * router logits are rounded to float32 before scoring, and the selection
     value is sigmoid rounded to float32 plus the float32 bias;
   * activation quantisation (scale = amax / 448, code = RNE_sat(v / scale))
@@ -35,7 +38,9 @@ exact int64 matmul (unit scales, integer activations), against a plain
 SwiGLU library routine with the limit at infinity, and against a dense average
 MLP when k = E with equal scores; the split-K GEMM against a float64 matmul;
 the MTP front's concatenation order and normalisation through projections
-that select one half (unit RMS of the selected half, the gathered row).
+that select one half (unit RMS of the selected half, the gathered row); the
+finalize's slot-to-row pairing through one-hot rows with distinct weights,
+and the routed scaling through the linearity of the routed part of m.
 The full layer on real shapes is pinned only through these pieces.
 """
 

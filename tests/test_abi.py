@@ -119,13 +119,30 @@ def test_layer_rejects_before_launch(L):
 
 def test_splitk_rejects_before_launch(L):
     fake = ctypes.c_void_p(0x10000)
-    assert L.splitk_gemm_bf16(fake, fake, fake, 0, 4, 7168, 100, 1.0, fake, 1 << 30, None) == m.MOE_ERR_UNSUPPORTED
-    assert L.splitk_gemm_bf16(fake, fake, fake, 0, 4, 7000, 14336, 1.0, fake, 1 << 30, None) == m.MOE_ERR_UNSUPPORTED
-    assert L.splitk_gemm_bf16(fake, fake, fake, 0, 300, 7168, 14336, 1.0, fake, 1 << 30, None) == m.MOE_ERR_UNSUPPORTED
-    assert L.splitk_gemm_bf16(None, fake, fake, 0, 4, 7168, 14336, 1.0, fake, 1 << 30, None) == m.MOE_ERR_INVALID_ARG
-    need = m.splitk_gemm_workspace_size(4, 7168, 14336)
-    assert L.splitk_gemm_bf16(fake, fake, fake, 0, 4, 7168, 14336, 1.0, fake, need - 1, None) == \
-        m.MOE_ERR_WORKSPACE_TOO_SMALL
+    call = lambda A, M, N, K, split, ws_bytes: L.splitk_gemm_bf16(A, fake, fake, 0, M, N, K, split, 1.0, fake,
+                                                                 ws_bytes, None)
+    assert call(fake, 4, 7168, 100, 0, 1 << 30) == m.MOE_ERR_UNSUPPORTED      # K % 128
+    assert call(fake, 4, 7000, 14336, 0, 1 << 30) == m.MOE_ERR_UNSUPPORTED    # N % 16
+    assert call(fake, 300, 7168, 14336, 0, 1 << 30) == m.MOE_ERR_UNSUPPORTED  # M > 256
+    assert call(None, 4, 7168, 14336, 0, 1 << 30) == m.MOE_ERR_INVALID_ARG
+    # split_k: negative is invalid, more segments than k-blocks unsupported
+    assert call(fake, 4, 7168, 14336, -1, 1 << 30) == m.MOE_ERR_INVALID_ARG
+    assert call(fake, 4, 7168, 14336, 113, 1 << 30) == m.MOE_ERR_UNSUPPORTED
+    n = ctypes.c_size_t(0)
+    assert L.splitk_gemm_workspace_size(4, 7168, 14336, -1, ctypes.byref(n)) == m.MOE_ERR_INVALID_ARG
+    assert L.splitk_gemm_workspace_size(4, 7168, 14336, 113, ctypes.byref(n)) == m.MOE_ERR_UNSUPPORTED
+    for split in (0, 1, 7, 112):
+        need = m.splitk_gemm_workspace_size(4, 7168, 14336, split)
+        assert call(fake, 4, 7168, 14336, split, need - 1) == m.MOE_ERR_WORKSPACE_TOO_SMALL
+    # an explicit split needs exactly its partial sums: tiles x S x 8 tokens x 64 rows (fp32),
+    # none when no tile is split, plus one counter per tile (rounded up to 256 bytes)
+    tiles = 7168 // 64
+    counters = (tiles * 4 + 255) // 256 * 256
+    assert m.splitk_gemm_workspace_size(4, 7168, 14336, 1) == counters
+    assert m.splitk_gemm_workspace_size(4, 7168, 14336, 7) == counters + tiles * 7 * 8 * 64 * 4
+    nz = L.splitk_gemm_bf16_noalloc
+    assert nz(fake, fake, fake, 0, 4, 7168, 14336, 113, 1.0, None) == m.MOE_ERR_UNSUPPORTED
+    assert nz(fake, fake, fake, 0, 4, 7168, 14336, -2, 1.0, None) == m.MOE_ERR_INVALID_ARG
 
 
 def test_mtp_front_rejects_before_launch(L):
@@ -139,7 +156,7 @@ def test_mtp_front_rejects_before_launch(L):
     assert call(fake, 0, 1e-6, 4, 7168, 1 << 30) == m.MOE_ERR_INVALID_ARG
     assert call(fake, 1000, -1.0, 4, 7168, 1 << 30) == m.MOE_ERR_INVALID_ARG
     need = m.mtp_eh_front_workspace_size(4, 7168)
-    assert need >= 256 + 4 * 2 * 7168 * 2 + m.splitk_gemm_workspace_size(4, 7168, 14336)
+    assert need >= 256 + 4 * 2 * 7168 * 2 + m.splitk_gemm_workspace_size(4, 7168, 14336, 0)
     assert call(fake, 1000, 1e-6, 4, 7168, need - 1) == m.MOE_ERR_WORKSPACE_TOO_SMALL
 
 

@@ -342,3 +342,40 @@ def test_dense_layer_is_the_moe_layer_without_routed_weight():
     d = orc.moe_decode_layer(dense, to_np(x), to_np(res))
     assert np.array_equal(d["out"], moe["out"]) and np.array_equal(d["residual_out"], moe["residual_out"])
     assert d["ids"].shape == (5, 0) and np.any(d["out"] != 0)
+
+
+# ------------------------------------------------------------ finalize
+
+def test_finalize_pairs_each_slot_with_its_own_row():
+    # one-hot rows: row r = t*k + j is the unit vector of column r, and slot j
+    # of token t carries weight j + 1.  Then m[t, t*k + j] must be j + 1 and
+    # every other column of token t zero; pairing slot j with the row of
+    # another slot, or another token's rows, moves or changes those values.
+    M, k = 3, 4
+    H = M * k + 2
+    rows = np.eye(M * k, H)
+    w = np.tile(np.arange(1, k + 1, dtype=np.float64), (M, 1))
+    m = orc.finalize(rows, w, None)
+    want = np.zeros((M, H))
+    for t in range(M):
+        for j in range(k):
+            want[t, t * k + j] = j + 1
+    assert np.array_equal(m, want)
+    # the shared output adds once per token, unweighted
+    shared = np.arange(M * H, dtype=np.float64).reshape(M, H)
+    assert np.array_equal(orc.finalize(rows, w, shared), want + shared)
+
+
+def test_routed_part_scales_linearly_with_routed_scaling():
+    # the routed scaling multiplies the routed weights only: with the ids
+    # unchanged (selection ignores the scaling), m - shared scales by the
+    # ratio of the two factors, and the shared expert's output does not
+    lw = synth.make_layer(TINY, seed=6)
+    x, res, _ = tie_free_tokens(TINY, lw, 3, seed=6)
+    a = orc.moe_decode_layer(oracle_layer(TINY.with_(routed_scaling=2.5), lw), to_np(x), to_np(res))
+    b = orc.moe_decode_layer(oracle_layer(TINY.with_(routed_scaling=1.0), lw), to_np(x), to_np(res))
+    assert np.array_equal(a["ids"], b["ids"])
+    assert np.array_equal(a["shared"], b["shared"]) and np.abs(a["shared"]).max() > 0.1
+    ra, rb = a["m"] - a["shared"], b["m"] - b["shared"]
+    assert np.abs(rb).max() > 0.01
+    assert np.allclose(ra, 2.5 * rb, rtol=1e-12, atol=1e-12)
