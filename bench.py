@@ -757,7 +757,7 @@ def run_ours(args, world, rank, local):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": round(exp_bytes_all / (len(MS) * args.steps))},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes},
-        "gpu_launches": m.LAUNCHES_PER_LAYER * len(MS) * args.steps,
+        "gpu_launches": sum(m.moe_decode_layer_plan(dims, M)[1] for M in MS) * args.steps,
         "timing": "value: events around each plain layer call; per-kernel us and roofline: a second, traced pass",
         "clocks": clk,
         "cpu_baseline": cpu,

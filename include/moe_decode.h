@@ -139,8 +139,14 @@ int moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
  *   workspace        from moe_decode_workspace_size(dims, max_tokens >= M),
  *                    zeroed once by moe_workspace_init; one workspace must not
  *                    be used by two calls that may run concurrently
- * M == 0 is a no-op.  Launches exactly three kernels (router + top-k + route
- * order; the expert kernel; finalize + residual + RMSNorm).
+ * M == 0 is a no-op.  Launches three kernels (router + top-k + route order;
+ * the expert kernel; finalize + residual + RMSNorm), four when the
+ * tensor-core expert kernel serves an MoE layer (the routed tokens' x codes
+ * are first gathered in route order); moe_decode_layer_plan reports which.
+ * The expert kernel is the warp-MMA kernel for narrow steps and the tcgen05
+ * kernel where an expert's tokens make a real contraction (a dense layer above
+ * 8 tokens, an MoE layer from 64 tokens); both compute the same results up to
+ * fp32 summation order.
  *
  * Dense layers ([decode page] LayerStages._build_dense: a dense FP8 MLP run as
  * GEMVs): num_experts = 0, top_k = 0, inter = 0 and the MLP's weights in the
@@ -157,8 +163,9 @@ int moe_decode_layer(const moe_layer_dims *dims, const moe_layer_weights *w, int
 
 /* moe_decode_layer that also records four CUDA events (cudaEvent_t passed as
  * void*) on `stream`: events[0] before the router kernel, [1] before the
- * expert kernel, [2] before the boundary kernel, [3] after it, so that a
- * caller can time each kernel.  The events are created by the caller. */
+ * expert phase (the gather of routed rows, when it runs, and the expert
+ * kernel), [2] before the boundary kernel, [3] after it, so that a caller can
+ * time each phase.  The events are created by the caller. */
 int moe_decode_layer_traced(const moe_layer_dims *dims, const moe_layer_weights *w, int M,
                             const void *x, const void *residual, void *out, void *residual_out,
                             int32_t *topk_ids, float *topk_w, int32_t *sorted_routes,
@@ -257,6 +264,25 @@ int mtp_eh_front_workspace_size(int M, int H, size_t *bytes);
 int mtp_eh_front(const int32_t *input_ids, const void *embed, int vocab, const void *hidden,
                  const void *enorm, const void *hnorm, float eps, const void *eh_proj_w, int M, int H,
                  void *out, void *ws, size_t ws_bytes, void *stream);
+
+/* Expert kernels (moe_decode_layer_plan, moe_set_expert_path). */
+enum moe_expert_path {
+  MOE_PATH_AUTO = 0,      /* the library's choice by layer kind and token count */
+  MOE_PATH_WARP_MMA = 1,  /* warp-level FP8 MMAs on 8/16/32-token passes       */
+  MOE_PATH_TCGEN05 = 2    /* tcgen05 FP8 MMAs, tensor-memory accumulators,
+                             passes of up to 64 tokens                          */
+};
+
+/* The expert kernel a moe_decode_layer call of M tokens runs (*path, never
+ * MOE_PATH_AUTO for M > 0) and the number of kernels it launches
+ * (*launches).  Host only. */
+int moe_decode_layer_plan(const moe_layer_dims *dims, int M, int *path, int *launches);
+
+/* Tuning and test hook: force the expert kernel of every later
+ * moe_decode_layer call in the process (MOE_PATH_AUTO restores the library's
+ * choice).  Process-wide; not meant to change while calls are being made
+ * from other host threads. */
+int moe_set_expert_path(int path);
 
 /* Read and clear the device status word of a moe_decode_layer workspace:
  * MOE_OK, or MOE_ERR_DEVICE_TIMEOUT when a bounded wait inside the expert

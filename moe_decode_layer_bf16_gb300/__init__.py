@@ -30,8 +30,10 @@ MOE_ERR_CUDA = 4
 MOE_ERR_DEVICE_TIMEOUT = 5
 MOE_ERR_SCRATCH_LIMIT = 6
 
-# kernels one moe_decode_layer call launches (router, experts, boundary)
-LAUNCHES_PER_LAYER = 3
+MOE_PATH_AUTO = 0
+MOE_PATH_WARP_MMA = 1
+MOE_PATH_TCGEN05 = 2
+
 
 
 class MoeError(RuntimeError):
@@ -78,6 +80,8 @@ def lib() -> ctypes.CDLL:
         L.rmsnorm_residual.argtypes = [_vp, _vp, _vp, _i, _i, _f, _vp, _vp, _i, _vp, _vp, _vp, _vp]
         L.mtp_eh_front_workspace_size.argtypes = [_i, _i, ctypes.POINTER(_sz)]
         L.mtp_eh_front.argtypes = [_vp, _vp, _i, _vp, _vp, _vp, _f, _vp, _i, _i, _vp, _vp, _sz, _vp]
+        L.moe_decode_layer_plan.argtypes = [ctypes.POINTER(_Dims), _i, ctypes.POINTER(_i), ctypes.POINTER(_i)]
+        L.moe_set_expert_path.argtypes = [_i]
         L.moe_device_status.argtypes = [_vp, _vp]
         L.moe_debug_set_fault.argtypes = [_vp, _i, _vp]
         L.moe_status_str.argtypes = [_i]
@@ -85,6 +89,7 @@ def lib() -> ctypes.CDLL:
         for n in ("moe_decode_workspace_size", "moe_workspace_init", "moe_decode_layer", "moe_decode_layer_traced",
                   "splitk_gemm_workspace_size", "splitk_gemm_bf16", "splitk_gemm_bf16_noalloc", "rmsnorm_residual",
                   "moe_device_status", "moe_debug_set_fault", "moe_debug_fill_noalloc_scratch",
+                  "moe_decode_layer_plan", "moe_set_expert_path",
                   "mtp_eh_front_workspace_size", "mtp_eh_front"):
             getattr(L, n).restype = ctypes.c_int
         _lib = L
@@ -231,6 +236,19 @@ def rmsnorm_residual(residual, gain, out, residual_out, eps: float, x=None, rows
                                 _ptr(route_w), k, _ptr(shared), _ptr(out), _ptr(residual_out),
                                 _stream(stream))
     _check(rc, "rmsnorm_residual")
+
+
+def moe_decode_layer_plan(dims: LayerDims, M: int):
+    """(expert kernel path, kernels launched) of a moe_decode_layer call of M tokens."""
+    path, n = _i(0), _i(0)
+    _check(lib().moe_decode_layer_plan(ctypes.byref(_dims(dims)), int(M), ctypes.byref(path), ctypes.byref(n)),
+           "moe_decode_layer_plan")
+    return path.value, n.value
+
+
+def moe_set_expert_path(path: int):
+    """Force the expert kernel of later calls (MOE_PATH_AUTO: the library's choice)."""
+    _check(lib().moe_set_expert_path(int(path)), "moe_set_expert_path")
 
 
 def moe_device_status(workspace, stream=None) -> int:

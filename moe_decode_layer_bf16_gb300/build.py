@@ -13,7 +13,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_decode.so")
-SOURCES = ["api.cu", "gemv.cu", "experts.cu", "rmsnorm.cu", "mtp.cu"]
+SOURCES = ["api.cu", "gemv.cu", "experts.cu", "experts_tc.cu", "rmsnorm.cu", "mtp.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--threads", "1"]
 

@@ -36,9 +36,31 @@ size_t gemv_partials_bound(int M, int N, int K) {
 
 struct Layout {
   size_t hdr, tickets, gcount, ready, partials, logits, xq, xs, ids, tw, sorted, off, act;
-  size_t h, hq, hs, rows, shared, total;
+  size_t h, hq, hs, rows, shared, xg, total;
   int n_gcount, n_ready, Imax, gI, hsS;
 };
+
+// Rows of the shared output region for M tokens: the tensor-core kernel may
+// split a dense layer's w2 items into K segments (partial rows the boundary
+// adds) while one pass holds all tokens; bounded so that the region grows
+// with M.
+size_t shared_rows(const moe_layer_dims& d, int M) {
+  const int segs = tc_shared_segments(d.shared_inter, 1);
+  return (size_t)std::max<long long>(M, (long long)segs * std::min(M, 64));
+}
+
+// Which expert kernel a call runs (moe_set_expert_path overrides the choice):
+// the tensor-core kernel where an expert's tokens make a real contraction (a
+// dense layer above 8 tokens, an MoE layer from 64 tokens), else the
+// warp-MMA kernel.
+std::atomic<int> g_path_override{0};
+
+int expert_path(const moe_layer_dims& d, int M) {
+  const int o = g_path_override.load(std::memory_order_relaxed);
+  if (o == MOE_PATH_WARP_MMA || o == MOE_PATH_TCGEN05) return o;
+  if (d.num_experts == 0) return M > 8 ? MOE_PATH_TCGEN05 : MOE_PATH_WARP_MMA;
+  return M >= 64 ? MOE_PATH_TCGEN05 : MOE_PATH_WARP_MMA;
+}
 
 void layout_for(const moe_layer_dims& d, int M, Layout& L) {
   const int H = d.hidden, E = d.num_experts, k = d.top_k;
@@ -67,7 +89,8 @@ void layout_for(const moe_layer_dims& d, int M, Layout& L) {
   L.hq = take(hrows * L.Imax);
   L.hs = take(hrows * L.hsS * sizeof(float));
   L.rows = take((size_t)M * k * H * sizeof(float));
-  L.shared = take((size_t)M * H * sizeof(float));
+  L.shared = take(shared_rows(d, M) * H * sizeof(float));
+  L.xg = take((size_t)M * k * H);
   L.total = o;
 }
 
@@ -259,12 +282,22 @@ static int layer_impl(const moe_layer_dims* dims, const moe_layer_weights* w, in
   // scale block) unless the rows are long (I >= 8192, a dense layer's MLP),
   // where single groups keep the queue's tail short
   ea.bq = L.Imax >= 8192 ? 1 : 4;
-  if (launch_experts(ea, sms, s) != cudaSuccess) return MOE_ERR_CUDA;
+  int parts = 1;
+  if (expert_path(*dims, M) == MOE_PATH_TCGEN05) {
+    // routed tokens' x rows in route order first (only the routing is waited for)
+    uint8_t* xg = ws + L.xg;
+    if (!dense && launch_gather_rows(ra.xq, ra.sorted, k, M * k, H, xg, sms, s) != cudaSuccess) return MOE_ERR_CUDA;
+    parts = tc_shared_segments(dims->shared_inter, M);
+    if (launch_experts_tc(ea, xg, parts, sms, s) != cudaSuccess) return MOE_ERR_CUDA;
+  } else if (launch_experts(ea, sms, s) != cudaSuccess) {
+    return MOE_ERR_CUDA;
+  }
   if (!mark(2)) return MOE_ERR_CUDA;
 
   NormArgs na;
   na.x = nullptr; na.residual = residual; na.gain = w->norm_gain;
   na.rows = ea.rows; na.route_w = ra.tw; na.shared = has_shared ? ea.shared_out : nullptr;
+  na.shared_parts = parts;
   na.out = out; na.residual_out = residual_out; na.M = M; na.H = H; na.k = k; na.eps = dims->rms_eps;
   // the residual and the gain were written before the router's plain launch,
   // so the boundary may load them before it waits on the expert kernel
@@ -336,7 +369,7 @@ int rmsnorm_residual(const void* x, const void* residual, const void* gain, int 
   if (M == 0) return MOE_OK;
   NormArgs na;
   na.x = x; na.residual = residual; na.gain = gain; na.rows = rows; na.route_w = route_w;
-  na.shared = shared; na.out = out; na.residual_out = residual_out; na.M = M; na.H = H;
+  na.shared = shared; na.shared_parts = 1; na.out = out; na.residual_out = residual_out; na.M = M; na.H = H;
   na.k = rows ? k : 0; na.eps = eps;
   na.early = 0;  // the preceding kernel may be the one that writes them
   return launch_rmsnorm(na, (cudaStream_t)stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
@@ -377,6 +410,22 @@ int mtp_eh_front(const int32_t* input_ids, const void* embed, int vocab, const v
   ea.status = reinterpret_cast<int*>(w) + kHdrStatus;
   if (launch_eh_norm(ea, (cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
   return splitk_gemm_bf16(A, eh_proj_w, out, 0, M, H, 2 * H, 0, 1.f, gemm_ws, need - (gemm_ws - w), stream);
+}
+
+int moe_set_expert_path(int path) {
+  if (path != MOE_PATH_AUTO && path != MOE_PATH_WARP_MMA && path != MOE_PATH_TCGEN05) return MOE_ERR_INVALID_ARG;
+  g_path_override.store(path, std::memory_order_relaxed);
+  return MOE_OK;
+}
+
+int moe_decode_layer_plan(const moe_layer_dims* dims, int M, int* path, int* launches) {
+  const int rc = check_dims(dims);
+  if (rc != MOE_OK) return rc;
+  if (M < 0 || !path || !launches) return MOE_ERR_INVALID_ARG;
+  if (M > kMaxTokens || (long long)M * dims->top_k > kMaxMk) return MOE_ERR_UNSUPPORTED;
+  *path = M == 0 ? MOE_PATH_AUTO : expert_path(*dims, M);
+  *launches = M == 0 ? 0 : (*path == MOE_PATH_TCGEN05 && dims->num_experts > 0 ? 4 : 3);
+  return MOE_OK;
 }
 
 int moe_device_status(void* ws, void* stream) {

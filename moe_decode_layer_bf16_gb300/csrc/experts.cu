@@ -42,8 +42,10 @@
 
 #include <algorithm>
 
+#include "async.cuh"
 #include "common.cuh"
 #include "kernels.h"
+#include "tmap.h"
 #include "../../include/moe_decode.h"
 
 namespace moe {
@@ -60,7 +62,6 @@ constexpr int kWHalf = 16384;
 constexpr int kXStride = 1088;            // gathered activation row pitch in a stage (1024 + 64)
 constexpr int kTabPer = 16;               // routing-table loads a producer lane keeps in flight
 constexpr int kSmemMax = 227 * 1024;
-constexpr unsigned long long kWaitNs = 200ull * 1000ull * 1000ull;
 
 // kFirst: first stage of a pass; kLast: last stage of a 32-row group (its
 // epilogue runs); kPassEnd: last stage of the pass; kSkip: nothing was copied
@@ -110,89 +111,6 @@ struct Cfg {
   }
   static constexpr int kNSTMax = 5;
 };
-
-// ------------------------------------------------------------- PTX wrappers
-MOE_DEV uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-MOE_DEV void mbar_init(uint64_t* b, int count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(b)), "r"(count) : "memory");
-}
-MOE_DEV void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(b)), "r"(bytes) : "memory");
-}
-MOE_DEV void mbar_arrive(uint64_t* b) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(su32(b)) : "memory");
-}
-MOE_DEV bool mbar_try_wait(uint64_t* b, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok) : "r"(su32(b)), "r"(parity) : "memory");
-  return ok != 0;
-}
-// Bounded wait for the phase of `parity` to complete; false (and the status
-// word set) when it did not within kWaitNs or when another wait already failed.
-MOE_DEV bool mbar_wait(uint64_t* b, uint32_t parity, int* status) {
-  if (mbar_try_wait(b, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  for (long it = 1; it < (1l << 26); ++it) {
-    if (mbar_try_wait(b, parity)) return true;
-    if ((it & 63) == 0) {
-      if (*(volatile int*)status != 0) return false;
-      if (globaltimer_ns() - t0 > kWaitNs) break;
-    }
-  }
-  atomicExch(status, MOE_ERR_DEVICE_TIMEOUT);
-  return false;
-}
-// Wait for copies this CTA has issued, bounded by time only: unlike mbar_wait
-// it does not give up when another wait of the grid has failed, because issued
-// copies always land and the CTA may not leave while one still writes into its
-// shared memory.  False (and the status word set) only when the bound ran out.
-MOE_DEV bool mbar_wait_landed(uint64_t* b, uint32_t parity, int* status) {
-  if (mbar_try_wait(b, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  for (long it = 1; it < (1l << 26); ++it) {
-    if (mbar_try_wait(b, parity)) return true;
-    if ((it & 63) == 0 && globaltimer_ns() - t0 > kWaitNs) break;
-  }
-  atomicExch(status, MOE_ERR_DEVICE_TIMEOUT);
-  return false;
-}
-MOE_DEV void tma_load_5d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3, int c4,
-                         uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(su32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(c2),
-      "r"(c3), "r"(c4), "r"(su32(bar))
-      : "memory");
-}
-MOE_DEV void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(su32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
-      "r"(su32(bar))
-      : "memory");
-}
-MOE_DEV void tma_load_3d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(su32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(su32(bar))
-      : "memory");
-}
-MOE_DEV void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(su32(dst)),
-      "l"(src), "r"(bytes), "r"(su32(bar))
-      : "memory");
-}
-MOE_DEV uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-// 16-byte chunk `c` of 128-byte row `f` of a tile written by TMA with the
-// 128-byte swizzle (chunk index XOR row index mod 8, rows 1024-byte aligned).
-MOE_DEV uint32_t swz(uint32_t base, int f, int c) { return base + f * 128 + ((c ^ (f & 7)) << 4); }
 
 // ------------------------------------------------------------- work items
 struct Slot {
@@ -254,16 +172,6 @@ struct TmaMaps {
   CUtensorMap xq;  // x codes [M][H/128][128], box 4 k-blocks x (tokens of a pass)
   CUtensorMap hq;  // h codes [Mk + M][Imax/128][128], same box
 };
-
-// L1-cached load of a block scale.  Weight and x scales are never written in
-// this kernel; an h-scale row is read only after its expert's ready signal and
-// is alone in its 128-byte line, so no stale line can be cached before it.
-MOE_DEV float ld_ca(const float* p) {
-  float v;
-  asm volatile("ld.global.ca.f32 %0, [%1];" : "=f"(v) : "l"(p));
-  return v;
-}
-
 
 template <int TT>
 __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArgs p, const __grid_constant__ TmaMaps maps,
@@ -805,23 +713,34 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
 }
 
 // ------------------------------------------------------------- host side
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+}  // namespace
 
 EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (!fn) {
+  // looked up once (a thread-safe static initialisation)
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
             cudaSuccess ||
         q != cudaDriverEntryPointSuccess)
       return nullptr;
-    fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
+    return reinterpret_cast<EncodeTiledFn>(ptr);
+  }();
   return fn;
 }
+
+bool tmap_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows) {
+  if (!encode_fn()) return false;
+  const cuuint64_t dim[2] = {cols, rows};
+  const cuuint64_t stride[1] = {cols};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dim, stride, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
 
 // w13 of n experts as [n][2][I][H/128][128] bytes; box = 16 rows of gate and up
 // x 4 k-blocks x 128 bytes.

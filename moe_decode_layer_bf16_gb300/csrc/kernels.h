@@ -118,11 +118,21 @@ struct ExpertArgs {
 };
 cudaError_t launch_experts(const ExpertArgs& a, int num_sms, cudaStream_t s);
 
+// The tensor-core (tcgen05) form of the expert kernel for wide passes: xg
+// holds the routed tokens' x codes in route order (written by
+// launch_gather_rows), sh_segs the K segments of the shared slot's w2 items
+// (tc_shared_segments), whose partial rows follow one another in shared_out.
+cudaError_t launch_experts_tc(const ExpertArgs& a, const uint8_t* xg, int sh_segs, int num_sms, cudaStream_t s);
+cudaError_t launch_gather_rows(const uint8_t* xq, const int* sorted, int k, int Mk, int H, uint8_t* xg, int num_sms,
+                               cudaStream_t s);
+int tc_shared_segments(int Is, int M);
+
 struct NormArgs {
   const void* x; const void* residual; const void* gain;
   const float* rows; const float* route_w; const float* shared;
   void* out; void* residual_out;
   int M, H, k;
+  int shared_parts;  // partial rows [parts][M][H] in `shared`, added in order (>= 1)
   float eps;
   int early;  // residual and gain come from before the preceding kernels (the layer call)
 };

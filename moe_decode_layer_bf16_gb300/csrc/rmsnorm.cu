@@ -90,8 +90,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 2)
       }
     }
     if (a.shared) {
-      const float4 r = *reinterpret_cast<const float4*>(a.shared + rowo + j);
-      m[0] += r.x; m[1] += r.y; m[2] += r.z; m[3] += r.w;
+      for (int pp = 0; pp < a.shared_parts; ++pp) {
+        const float4 r = *reinterpret_cast<const float4*>(a.shared + (size_t)pp * a.M * a.H + rowo + j);
+        m[0] += r.x; m[1] += r.y; m[2] += r.z; m[3] += r.w;
+      }
     }
     const float r0 = m[0] + bf16_lo(rv[i].x), r1 = m[1] + bf16_hi(rv[i].x);
     const float r2 = m[2] + bf16_lo(rv[i].y), r3 = m[3] + bf16_hi(rv[i].y);

@@ -178,3 +178,33 @@ def test_product_path_has_no_oracle_import():
             if f.endswith((".py", ".cu", ".cuh", ".h")):
                 src = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"(import\s+oracle|from\s+oracle|oracle[./]|moe_oracle)", src), f
+
+
+def test_layer_plan_and_path_override(L):
+    from moe_decode_layer_bf16_gb300.dims import DSV3_DENSE
+    assert m.moe_decode_layer_plan(DSV3, 1) == (m.MOE_PATH_WARP_MMA, 3)
+    assert m.moe_decode_layer_plan(DSV3, 32) == (m.MOE_PATH_WARP_MMA, 3)
+    assert m.moe_decode_layer_plan(DSV3, 64) == (m.MOE_PATH_TCGEN05, 4)  # + the gather of routed rows
+    assert m.moe_decode_layer_plan(DSV3_DENSE, 8) == (m.MOE_PATH_WARP_MMA, 3)
+    assert m.moe_decode_layer_plan(DSV3_DENSE, 9) == (m.MOE_PATH_TCGEN05, 3)
+    assert m.moe_decode_layer_plan(DSV3, 0) == (m.MOE_PATH_AUTO, 0)
+    try:
+        m.moe_set_expert_path(m.MOE_PATH_TCGEN05)
+        assert m.moe_decode_layer_plan(DSV3, 1) == (m.MOE_PATH_TCGEN05, 4)
+        m.moe_set_expert_path(m.MOE_PATH_WARP_MMA)
+        assert m.moe_decode_layer_plan(DSV3, 256) == (m.MOE_PATH_WARP_MMA, 3)
+    finally:
+        m.moe_set_expert_path(m.MOE_PATH_AUTO)
+    assert L.moe_set_expert_path(3) == m.MOE_ERR_INVALID_ARG
+    p, n = ctypes.c_int(0), ctypes.c_int(0)
+    assert L.moe_decode_layer_plan(ctypes.byref(m._dims(DSV3)), 600, ctypes.byref(p), ctypes.byref(n)) == \
+        m.MOE_ERR_UNSUPPORTED
+
+
+def test_workspace_covers_split_dense_rows(L):
+    # a dense layer's w2 items may be split into K segments whose partial rows
+    # the boundary adds: the workspace holds them and never shrinks as M grows
+    from moe_decode_layer_bf16_gb300.dims import DSV3_DENSE
+    sizes = [m.moe_decode_workspace_size(DSV3_DENSE, t) for t in range(60, 70)]
+    assert sizes == sorted(sizes)
+    assert sizes[4] >= 9 * 64 * 7168 * 4  # 64 tokens, 9 segments of fp32 rows
