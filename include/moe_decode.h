@@ -144,9 +144,9 @@ int moe_workspace_init(void *ws, size_t ws_bytes, void *stream);
  * tensor-core expert kernel serves an MoE layer (the routed tokens' x codes
  * are first gathered in route order); moe_decode_layer_plan reports which.
  * The expert kernel is the warp-MMA kernel for narrow steps and the tcgen05
- * kernel where an expert's tokens make a real contraction (a dense layer above
- * 8 tokens, an MoE layer from 64 tokens); both compute the same results up to
- * fp32 summation order.
+ * kernel where an expert's tokens can make a real contraction (a dense layer
+ * from 4 tokens, an MoE layer from 16 tokens); both compute the same results
+ * up to fp32 summation order and the SwiGLU's exponential.
  *
  * Dense layers ([decode page] LayerStages._build_dense: a dense FP8 MLP run as
  * GEMVs): num_experts = 0, top_k = 0, inter = 0 and the MLP's weights in the

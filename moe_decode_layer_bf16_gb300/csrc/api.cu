@@ -36,7 +36,7 @@ size_t gemv_partials_bound(int M, int N, int K) {
 
 struct Layout {
   size_t hdr, tickets, gcount, ready, partials, logits, xq, xs, ids, tw, sorted, off, act;
-  size_t h, hq, hs, rows, shared, xg, total;
+  size_t h, hq, hs, rows, shared, xg, gu_part, total;
   int n_gcount, n_ready, Imax, gI, hsS;
 };
 
@@ -45,21 +45,24 @@ struct Layout {
 // adds) while one pass holds all tokens; bounded so that the region grows
 // with M.
 size_t shared_rows(const moe_layer_dims& d, int M) {
-  const int segs = tc_shared_segments(d.shared_inter, 1);
-  return (size_t)std::max<long long>(M, (long long)segs * std::min(M, 64));
+  // (at most kMaxSharedSegs segments, whatever the SM count)
+  const int segs = std::max(1, std::min(kMaxSharedSegs, d.shared_inter / kBlock));
+  return (size_t)std::max<long long>(M, (long long)(d.num_experts == 0 ? segs : 1) * std::min(M, 64));
 }
 
 // Which expert kernel a call runs (moe_set_expert_path overrides the choice):
-// the tensor-core kernel where an expert's tokens make a real contraction (a
-// dense layer above 8 tokens, an MoE layer from 64 tokens), else the
+// the tensor-core kernel where the tokens of an expert can make a real
+// contraction (a dense layer from 4 tokens, an MoE layer from 16 tokens:
+// measured on the DeepSeek-V3-shaped layers, where below these counts the
+// warp-MMA kernel's finer items start the routed w2 work sooner), else the
 // warp-MMA kernel.
 std::atomic<int> g_path_override{0};
 
 int expert_path(const moe_layer_dims& d, int M) {
   const int o = g_path_override.load(std::memory_order_relaxed);
   if (o == MOE_PATH_WARP_MMA || o == MOE_PATH_TCGEN05) return o;
-  if (d.num_experts == 0) return M > 8 ? MOE_PATH_TCGEN05 : MOE_PATH_WARP_MMA;
-  return M >= 64 ? MOE_PATH_TCGEN05 : MOE_PATH_WARP_MMA;
+  if (d.num_experts == 0) return M >= 4 ? MOE_PATH_TCGEN05 : MOE_PATH_WARP_MMA;
+  return M >= 16 ? MOE_PATH_TCGEN05 : MOE_PATH_WARP_MMA;
 }
 
 void layout_for(const moe_layer_dims& d, int M, Layout& L) {
@@ -67,7 +70,7 @@ void layout_for(const moe_layer_dims& d, int M, Layout& L) {
   L.Imax = std::max(d.inter, d.shared_inter);
   L.gI = L.Imax / kBlock;
   L.hsS = (L.gI + 31) / 32 * 32;
-  L.n_gcount = (E + 1) * L.gI;
+  L.n_gcount = 2 * (E + 1) * L.gI;  // the expert kernels' group counters, then the split-segment counts
   L.n_ready = E + 1;
   size_t o = 0;
   auto take = [&](size_t bytes) { const size_t at = o; o = align_up(o + bytes); return at; };
@@ -91,6 +94,7 @@ void layout_for(const moe_layer_dims& d, int M, Layout& L) {
   L.rows = take((size_t)M * k * H * sizeof(float));
   L.shared = take(shared_rows(d, M) * H * sizeof(float));
   L.xg = take((size_t)M * k * H);
+  L.gu_part = take(tc_w13_partial_bytes(E, d.shared_inter));
   L.total = o;
 }
 
@@ -257,13 +261,6 @@ static int layer_impl(const moe_layer_dims* dims, const moe_layer_weights* w, in
   ra.ready = reinterpret_cast<int*>(ws + L.ready);
   ra.n_ready = L.n_ready;
   ra.user_ids = topk_ids; ra.user_w = topk_w; ra.user_sorted = sorted_routes; ra.user_off = expert_offsets;
-  auto mark = [&](int i) {
-    return !events || cudaEventRecord((cudaEvent_t)events[i], s) == cudaSuccess;
-  };
-  if (!mark(0)) return MOE_ERR_CUDA;
-  if (launch_router(plan, ra, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (!mark(1)) return MOE_ERR_CUDA;
-
   ExpertArgs ea;
   ea.H = H; ea.I = dims->inter; ea.Is = dims->shared_inter; ea.E = E; ea.k = k; ea.M = M; ea.Mk = M * k;
   ea.Imax = L.Imax; ea.gI = L.gI; ea.hsS = L.hsS;
@@ -282,16 +279,29 @@ static int layer_impl(const moe_layer_dims* dims, const moe_layer_weights* w, in
   // scale block) unless the rows are long (I >= 8192, a dense layer's MLP),
   // where single groups keep the queue's tail short
   ea.bq = L.Imax >= 8192 ? 1 : 4;
-  int parts = 1;
-  if (expert_path(*dims, M) == MOE_PATH_TCGEN05) {
-    // routed tokens' x rows in route order first (only the routing is waited for)
-    uint8_t* xg = ws + L.xg;
-    if (!dense && launch_gather_rows(ra.xq, ra.sorted, k, M * k, H, xg, sms, s) != cudaSuccess) return MOE_ERR_CUDA;
-    parts = tc_shared_segments(dims->shared_inter, M);
-    if (launch_experts_tc(ea, xg, parts, sms, s) != cudaSuccess) return MOE_ERR_CUDA;
-  } else if (launch_experts(ea, sms, s) != cudaSuccess) {
+  // every expert-kernel launch parameter is prepared before the router is
+  // enqueued, so that no host work delays the expert kernel behind it
+  const bool tc = expert_path(*dims, M) == MOE_PATH_TCGEN05;
+  uint8_t* xg = ws + L.xg;
+  const int parts = tc ? tc_shared_segments(H, dims->shared_inter, M, sms) : 1;
+  TcExtra tx;
+  tx.xg = xg;
+  tx.sh_segs = parts;
+  tx.a_segs = tc_w13_segments(E, H, dims->shared_inter, M);
+  tx.gu_part = reinterpret_cast<float*>(ws + L.gu_part);
+  tx.pcount = ea.gcount + (E + 1) * L.gI;
+  ExpertsLaunch el;
+  if ((tc ? prepare_experts_tc(ea, tx, el) : prepare_experts(ea, el)) != cudaSuccess) return MOE_ERR_CUDA;
+  auto mark = [&](int i) {
+    return !events || cudaEventRecord((cudaEvent_t)events[i], s) == cudaSuccess;
+  };
+  if (!mark(0)) return MOE_ERR_CUDA;
+  if (launch_router(plan, ra, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!mark(1)) return MOE_ERR_CUDA;
+  // routed tokens' x rows in route order first (only the routing is waited for)
+  if (tc && !dense && launch_gather_rows(ra.xq, ra.sorted, k, M * k, H, xg, sms, s) != cudaSuccess)
     return MOE_ERR_CUDA;
-  }
+  if (launch_experts(el, sms, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (!mark(2)) return MOE_ERR_CUDA;
 
   NormArgs na;

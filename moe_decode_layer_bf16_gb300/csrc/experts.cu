@@ -784,29 +784,45 @@ bool map_rows(CUtensorMap* m, const uint8_t* base, int K, int rows, int box_rows
 }
 
 template <int TT>
-cudaError_t launch_tt(const ExpertArgs& a, TmaMaps& maps, int num_sms, cudaStream_t s) {
-  if (!map_rows(&maps.xq, a.xq, a.H, a.M, Cfg<TT>::kTok) || !map_rows(&maps.hq, a.hq, a.Imax, a.Mk + a.M, Cfg<TT>::kTok))
+cudaError_t prepare_tt(const ExpertArgs& a, ExpertsLaunch& L) {
+  TmaMaps* maps = reinterpret_cast<TmaMaps*>(L.maps);
+  if (!map_rows(&maps->xq, a.xq, a.H, a.M, Cfg<TT>::kTok) ||
+      !map_rows(&maps->hq, a.hq, a.Imax, a.Mk + a.M, Cfg<TT>::kTok))
     return cudaErrorInvalidValue;
   int nst = Cfg<TT>::kNSTMax;
   while (nst > 2 && (size_t)nst * Cfg<TT>::kSlot + other_smem<TT>(a, nst) > (size_t)kSmemMax) --nst;
   const size_t smem = (size_t)nst * Cfg<TT>::kSlot + other_smem<TT>(a, nst);
   if (smem > (size_t)kSmemMax) return cudaErrorInvalidConfiguration;
-  cudaError_t err = cudaFuncSetAttribute(experts_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
-  PdlLaunch L(dim3(num_sms), dim3(Cfg<TT>::kThreads), smem, s);
-  return cudaLaunchKernelEx(&L.cfg, experts_kernel<TT>, a, maps, nst);
+  L.tt = TT;
+  L.nst = nst;
+  L.smem = smem;
+  return cudaFuncSetAttribute(experts_kernel<TT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
+template <int TT>
+cudaError_t launch_tt(const ExpertsLaunch& L, int num_sms, cudaStream_t s) {
+  TmaMaps maps;
+  memcpy(&maps, L.maps, sizeof(maps));
+  PdlLaunch P(dim3(num_sms), dim3(Cfg<TT>::kThreads), L.smem, s);
+  return cudaLaunchKernelEx(&P.cfg, experts_kernel<TT>, L.a, maps, L.nst);
 }
 
 }  // namespace
 
-cudaError_t launch_experts(const ExpertArgs& a, int num_sms, cudaStream_t s) {
+static_assert(sizeof(TmaMaps) <= sizeof(ExpertsLaunch::maps), "tensor maps fit the prepared launch");
+
+cudaError_t launch_experts_tc_prepared(const ExpertsLaunch& L, int num_sms, cudaStream_t s);
+
+cudaError_t prepare_experts(const ExpertArgs& a, ExpertsLaunch& L) {
   if (!encode_fn()) return cudaErrorNotSupported;
-  TmaMaps maps;
-  memset(&maps, 0, sizeof(maps));
+  memset(&L, 0, sizeof(L));
+  L.a = a;
+  L.tc = false;
+  TmaMaps* maps = reinterpret_cast<TmaMaps*>(L.maps);
   // (a dense layer has no routed experts: their maps stay zero, never used)
-  if (a.E > 0 && (!map_w13(&maps.w13, a.w13, a.H, a.I, a.E) || !map_w2(&maps.w2, a.w2, a.H, a.I, a.E)))
+  if (a.E > 0 && (!map_w13(&maps->w13, a.w13, a.H, a.I, a.E) || !map_w2(&maps->w2, a.w2, a.H, a.I, a.E)))
     return cudaErrorInvalidValue;
-  if (a.Is > 0 && (!map_w13(&maps.sw13, a.sw13, a.H, a.Is, 1) || !map_w2(&maps.sw2, a.sw2, a.H, a.Is, 1)))
+  if (a.Is > 0 && (!map_w13(&maps->sw13, a.sw13, a.H, a.Is, 1) || !map_w2(&maps->sw2, a.sw2, a.H, a.Is, 1)))
     return cudaErrorInvalidValue;
   // Passes of 8 tokens: an expert with more tokens (the shared expert above
   // M = 8) streams its rows once per pass, the repeats from L2.  Wider passes
@@ -815,12 +831,21 @@ cudaError_t launch_experts(const ExpertArgs& a, int num_sms, cudaStream_t s) {
   if (a.E == 0) {
     // a dense layer: every token goes through the one MLP, so the widest pass
     // streams its weights the fewest times
-    if (a.M <= 8) return launch_tt<1>(a, maps, num_sms, s);
-    if (a.M <= 16) return launch_tt<2>(a, maps, num_sms, s);
-    return launch_tt<4>(a, maps, num_sms, s);
+    if (a.M <= 8) return prepare_tt<1>(a, L);
+    if (a.M <= 16) return prepare_tt<2>(a, L);
+    return prepare_tt<4>(a, L);
   }
-  if (a.M <= 128) return launch_tt<1>(a, maps, num_sms, s);
-  return launch_tt<2>(a, maps, num_sms, s);
+  if (a.M <= 128) return prepare_tt<1>(a, L);
+  return prepare_tt<2>(a, L);
+}
+
+cudaError_t launch_experts(const ExpertsLaunch& L, int num_sms, cudaStream_t s) {
+  if (L.tc) return launch_experts_tc_prepared(L, num_sms, s);
+  switch (L.tt) {
+    case 1: return launch_tt<1>(L, num_sms, s);
+    case 2: return launch_tt<2>(L, num_sms, s);
+    default: return launch_tt<4>(L, num_sms, s);
+  }
 }
 
 }  // namespace moe

@@ -67,10 +67,36 @@ constexpr int kNST = 4;                  // ring stages
 constexpr int kTCols = 512;              // tensor-memory columns: kNST accumulator pairs of 2 x kPass
 constexpr int kMetaInts = 8;
 constexpr int kThreads = 12 * 32;
-constexpr int kPW = 0, kMW = 1, kEW0 = 4, kNEpi = 8;
-constexpr int kSegKB = 16;               // k-blocks of a w2 item's K segment, when I is split
+constexpr int kPW = 0, kMW = 1, kSW = 2, kEW0 = 4, kNEpi = 8;
+// Tuning constants of a dense layer's item split (measured on the DeepSeek-V3
+// dense MLP; overridable at build time for sweeps).
+#ifndef MOE_TC_W2_SEG_WAVES
+#define MOE_TC_W2_SEG_WAVES 3
+#endif
+#ifndef MOE_TC_W13_SEGS
+#define MOE_TC_W13_SEGS 1
+#endif
+constexpr int kSegWaves = MOE_TC_W2_SEG_WAVES;  // w2 items per SM, when a dense layer's I is split
+constexpr int kW13Segs = MOE_TC_W13_SEGS; // K segments of a dense layer's w13 items
 
 static_assert(kNST * 2 * kPass == kTCols, "one accumulator pair per ring stage");
+
+// Shared-memory carve-up (byte offsets from the 1024-byte aligned base), used
+// by the kernel and by the launch's size alike.
+constexpr size_t align_to(size_t x, size_t a) { return (x + a - 1) / a * a; }
+struct SmemTc {
+  static constexpr size_t kMeta = (size_t)kNST * kSlotB;                        // stage descriptors
+  static constexpr size_t kTmeta = kMeta + (size_t)kNST * kMetaInts * 4;        // accumulator descriptors
+  static constexpr size_t kBars = kTmeta + (size_t)kNST * kMetaInts * 4;        // mbarriers
+  static constexpr int kNBars = 6 * kNST + 4 + 3;
+  static constexpr size_t kCstage = align_to(kBars + (size_t)kNBars * 8, 16);   // scale products (float4 reads)
+  static constexpr size_t kAmax = kCstage + (size_t)kNST * 2 * kPass * 4;       // amax exchange
+  static constexpr size_t kMisc = kAmax + 2 * 2 * 4 * 32 * 4;                    // misc words, then the tables
+  static constexpr size_t bytes(int E) { return 1024 + kMisc + (size_t)(4 + 2 * E + 1) * 4; }
+};
+static_assert(SmemTc::kMeta % 1024 == 0 && SmemTc::kMeta % 16 == 0, "ring tiles 1024-aligned, descriptors 16");
+static_assert(SmemTc::kTmeta % 16 == 0 && SmemTc::kBars % 8 == 0, "descriptor and barrier alignment");
+static_assert(SmemTc::kCstage % 16 == 0 && SmemTc::kAmax % 16 == 0, "vector-read alignment");
 
 // stage flags
 enum TcFlag { kFA = 1, kFFirst = 2, kFLast = 4, kFEnd = 8, kFFinal = 16 };
@@ -99,27 +125,33 @@ MOE_DEV void tc_commit(uint64_t* bar) {
 }
 MOE_DEV void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 MOE_DEV void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-// 32 consecutive fp32 columns of this thread's lane
-MOE_DEV void tc_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+// 16 consecutive fp32 columns of this thread's lane, without waiting: the
+// registers are valid after tc_wait_ld()
+MOE_DEV void tc_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
+  for (int j = 0; j < 16; ++j) v[j] = __uint_as_float(r[j]);
 }
+MOE_DEV void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // Bounded wait that ignores the status word (the waits of the MMA and
 // epilogue warps end together, by the phase or by the bound).
 MOE_DEV bool mbar_wait_t(uint64_t* b, uint32_t parity, int* status) { return mbar_wait_landed(b, parity, status); }
 
 // ------------------------------------------------------------- work items
+struct TcArgs {
+  const uint8_t* xg;
+  int sh_segs;     // K segments of the shared slot's w2 items (partial rows the boundary adds)
+  int a_segs;      // K segments of the shared slot's w13 items (partial [g; u] rows in gu_part)
+  float* gu_part;  // [group][segment][gate | up][kPass columns][128 rows] fp32
+  int* pcount;     // [group] segments of the group done
+};
+
 struct TcItem {
   bool a;
   int slot, idx, seg;  // idx: 128-intermediate block (A) or 128-row block of w2 (B); seg: K segment (B)
@@ -133,27 +165,31 @@ struct TcSlot {
   int e;      // routed expert id, -1 for the shared expert
 };
 
-MOE_DEV TcItem tc_decode(int item, int nA_sh, int nA_r, int totA, int nB, int sh_segs, bool has_shared) {
+// A items: the shared slot's (128-intermediate block, K segment) pairs, then
+// each routed expert's blocks; B items: the shared slot's (128-row block, K
+// segment) pairs, then each routed expert's row blocks.
+MOE_DEV TcItem tc_decode(int item, int nA_sh, int nA_r, int totA, int nB, const TcArgs& q, bool has_shared) {
   TcItem it;
   if (item < totA) {
     it.a = true;
-    it.seg = 0;
     if (item < nA_sh) {
       it.slot = 0;
-      it.idx = item;
+      it.idx = item / q.a_segs;
+      it.seg = item % q.a_segs;
     } else {
       const int j = item - nA_sh;
       it.slot = j / nA_r + (has_shared ? 1 : 0);
       it.idx = j % nA_r;
+      it.seg = 0;
     }
   } else {
     it.a = false;
     int j = item - totA;
-    const int nBs = has_shared ? nB * sh_segs : 0;
+    const int nBs = has_shared ? nB * q.sh_segs : 0;
     if (j < nBs) {
       it.slot = 0;
-      it.idx = j / sh_segs;
-      it.seg = j % sh_segs;
+      it.idx = j / q.sh_segs;
+      it.seg = j % q.sh_segs;
     } else {
       j -= nBs;
       it.slot = j / nB + (has_shared ? 1 : 0);
@@ -175,18 +211,13 @@ MOE_DEV TcSlot tc_slot(const ExpertArgs& p, const int* s_off, const int* s_act, 
   return s;
 }
 
-// K range of an item, in k-blocks: all of H (A) or segment seg of Ie (B)
-MOE_DEV void tc_krange(const ExpertArgs& p, const TcItem& it, const TcSlot& s, int sh_segs, int& k0, int& k1) {
-  if (it.a) {
-    k0 = 0;
-    k1 = p.H / kBlock;
-    return;
-  }
-  const int nkb = s.Ie / kBlock;
-  const int segs = s.e < 0 ? sh_segs : 1;
-  const int len = (nkb + segs - 1) / segs;
-  k0 = it.seg * len;
-  k1 = min(nkb, k0 + len);
+// K range of an item, in k-blocks: segment seg of H (A) or of Ie (B)
+MOE_DEV void tc_krange(const ExpertArgs& p, const TcItem& it, const TcSlot& s, const TcArgs& q, int& k0, int& k1) {
+  const int nkb = it.a ? p.H / kBlock : s.Ie / kBlock;
+  const int segs = s.e < 0 ? (it.a ? q.a_segs : q.sh_segs) : 1;
+  // balanced: every segment holds at least one k-block (segs <= nkb)
+  k0 = it.seg * nkb / segs;
+  k1 = (it.seg + 1) * nkb / segs;
 }
 
 struct TcMaps {
@@ -196,10 +227,6 @@ struct TcMaps {
   CUtensorMap hq;                  // h codes [Mk + M][Imax]
 };
 
-struct TcArgs {
-  const uint8_t* xg;
-  int sh_segs;  // K segments of the shared slot's w2 items (partial rows the boundary adds)
-};
 
 __global__ void __launch_bounds__(kThreads, 1)
     experts_tc_kernel(ExpertArgs p, TcArgs q, const __grid_constant__ TcMaps maps) {
@@ -208,32 +235,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nkbH = p.H / kBlock;
 
-  // ---- shared memory: ring | stage descriptors | accumulator descriptors | barriers | epilogue buffers | tables
+  // ---- shared memory (offsets in SmemTc): ring | stage descriptors | accumulator descriptors |
+  //      barriers | scale products | amax exchange | tables
   uint8_t* ring = smem;
-  int* meta = reinterpret_cast<int*>(smem + (size_t)kNST * kSlotB);   // [kNST][kMetaInts]
-  int* tmeta = meta + kNST * kMetaInts;                                  // [kNST][kMetaInts]
-  uint64_t* full = reinterpret_cast<uint64_t*>(tmeta + kNST * kMetaInts);
+  int* meta = reinterpret_cast<int*>(smem + SmemTc::kMeta);      // [kNST][kMetaInts]
+  int* tmeta = reinterpret_cast<int*>(smem + SmemTc::kTmeta);    // [kNST][kMetaInts]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + SmemTc::kBars);
   uint64_t* empty = full + kNST;
   uint64_t* tfull = empty + kNST;
   uint64_t* tempty = tfull + kNST;
-  uint64_t* amax_bar = tempty + kNST;   // [2 pass parities][2 column halves]
+  uint64_t* mready = tempty + kNST;     // the producer has described the stage
+  uint64_t* sready = mready + kNST;     // the stage's scale products are in cstage
+  uint64_t* amax_bar = sready + kNST;   // [2 alternating buffers][2 column halves]
   uint64_t* mma_done = amax_bar + 4;
-  float* cbuf = reinterpret_cast<float*>(mma_done + 2);                 // [8 warps][2][32]
-  float* amax_buf = cbuf + kNEpi * 64;                                   // [2][2][4][32]
-  int* s_misc = reinterpret_cast<int*>(amax_buf + 2 * 2 * 4 * 32);       // [0] tensor-memory base, [1] routed experts
+  uint64_t* psync = mma_done + 1;       // split w13 items: the eight warps wrote their partial sums
+  uint64_t* pdec = psync + 1;           // split w13 items: whether this item completes its group
+  float* cstage = reinterpret_cast<float*>(smem + SmemTc::kCstage);    // [kNST][2 pairs][kPass columns]
+  float* amax_buf = reinterpret_cast<float*>(smem + SmemTc::kAmax);    // [2][2][4][32]
+  int* s_misc = reinterpret_cast<int*>(smem + SmemTc::kMisc);          // [0] tensor-memory base, [1] routed experts, [2] split decision
   int* s_off = s_misc + 4;                                               // [E+1]
   int* s_act = s_off + (p.E + 1);                                        // [E]
   int* status = p.hdr + kHdrStatus;
 
+  // the dynamic shared memory must start where the carve-up expects (checked
+  // once; the condition is the same in every thread, so all leave together)
+  if ((su32(ring) & 1023u) != 0) {
+    if (tid == 0) atomicExch(status, MOE_ERR_INVALID_ARG);
+    return;
+  }
   if (tid == 0) {
     for (int i = 0; i < kNST; ++i) {
       mbar_init(full + i, 1);    // the producer's expect-tx arrival
-      mbar_init(empty + i, 2);   // the MMAs' commit + the MMA thread
+      mbar_init(empty + i, 3);   // the MMAs' commit, the MMA thread, the scale warp (descriptor read)
       mbar_init(tfull + i, 2);   // the MMAs' commit + the MMA thread
       mbar_init(tempty + i, kNEpi);
+      mbar_init(mready + i, 1);
+      mbar_init(sready + i, 1);
     }
     for (int i = 0; i < 4; ++i) mbar_init(amax_bar + i, 4);
     mbar_init(mma_done, 1);
+    mbar_init(psync, kNEpi);
+    mbar_init(pdec, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_misc[1] = 0;
   }
@@ -251,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = (uint32_t)s_misc[0];
 
   const bool has_shared = p.Is > 0;
-  const int nA_sh = has_shared ? p.Is / kRows : 0;
+  const int nA_sh = has_shared ? p.Is / kRows * q.a_segs : 0;
   const int nA_r = p.I / kRows;
   const int nB = p.H / kRows;
 
@@ -303,12 +345,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         routed = true;
       }
       if (item >= total) break;
+      // the next item is claimed two stages before this one's last stage, not
+      // now: with few, long items a claim made at the start would hold an item
+      // that an idle CTA could run at once
       int nxt = 0;
-      if (lane == 0) nxt = atomicAdd(p.hdr + kHdrQueue, 1);
-      const TcItem it = tc_decode(item, nA_sh, nA_r, totA, nB, q.sh_segs, has_shared);
+      bool claimed = false;
+      const TcItem it = tc_decode(item, nA_sh, nA_r, totA, nB, q, has_shared);
       const TcSlot s = tc_slot(p, s_off, s_act, it.slot, has_shared);
       int k0, k1;
-      tc_krange(p, it, s, q.sh_segs, k0, k1);
+      tc_krange(p, it, s, q, k0, k1);
       if (!it.a && !all_ready) {
         // a w2 item needs its K range of h quantised: every A item done, or
         // each group of the range published by all eight epilogue warps
@@ -342,6 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int passes = (s.nt + kPass - 1) / kPass;
       const int kstep = it.a ? 1 : 2;
+      const int nstages = passes * ((k1 - k0 + kstep - 1) / kstep);
+      int stage = 0;
       for (int pass = 0; pass < passes && alive; ++pass) {
         const int ntok = min(kPass, s.nt - pass * kPass);
         const int npad = (ntok + 15) & ~15;
@@ -349,7 +396,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // x rows in route order (routed), h rows (w2)
         const CUtensorMap* xmap = it.a ? (s.e < 0 ? &maps.xq : &maps.xg) : &maps.hq;
         const int xrow = (it.a ? (s.e < 0 ? 0 : s.o) : s.hbase) + pass * kPass;
-        for (int kb = k0; kb < k1; kb += kstep) {
+        for (int kb = k0; kb < k1; kb += kstep, ++stage) {
+          if (!claimed && stage >= nstages - 3) {
+            if (lane == 0) nxt = atomicAdd(p.hdr + kHdrQueue, 1);
+            claimed = true;
+          }
           int ok = 1;
           if (lane == 0) ok = mbar_wait(empty + si, ph ^ 1u, status);
           __syncwarp();
@@ -362,6 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                            (kb + kstep >= k1 && pass == passes - 1 ? kFFinal : 0);
             *reinterpret_cast<int4*>(md) = make_int4(item, pass, kb, fl);
             *reinterpret_cast<int4*>(md + 4) = make_int4(ntok, npad, nkv, 0);
+            mbar_arrive(mready + si);  // the scale warp starts on the descriptor now
             const uint32_t xbytes = (uint32_t)(npad / 16) * 2048u;
             mbar_expect_tx(full + si, it.a ? 2u * kWTile + xbytes : (uint32_t)nkv * (kWTile + xbytes));
           }
@@ -387,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
       }
+      if (!claimed && lane == 0) nxt = atomicAdd(p.hdr + kHdrQueue, 1);  // (an item that stopped early)
       item = __shfl_sync(0xffffffffu, nxt, 0);
     }
     // end marker, then make sure every copy this CTA issued has landed
@@ -396,6 +449,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (__shfl_sync(0xffffffffu, ok, 0)) {
         if (lane == 0) {
           meta[kMetaInts * si + 3] = kFEnd;
+          mbar_arrive(mready + si);
           mbar_arrive(full + si);
         }
         ++gs;
@@ -453,42 +507,36 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp >= kEW0) {
-    // ================================================================ epilogue
-    const int ew = warp - kEW0;
-    const int qd = warp & 3;           // tensor-memory lane quadrant: rows 32 qd .. 32 qd + 31
-    const int hf = ew >> 2;            // token column half: columns 32 hf .. 32 hf + 31 of a pass
-    const int col0 = 32 * hf;
-    const int r = 32 * qd + lane;      // this thread's row of the 128-row tile
-    float* cb = cbuf + ew * 64;
-    float acc0[32], acc1[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) acc0[j] = acc1[j] = 0.f;
+  } else if (warp == kSW) {
+    // ================================================================ scale products
+    // For every stage, as soon as the producer has described it: the scale of
+    // each (pair, token column): weight block scale x token group scale, so
+    // that the epilogue reads them from shared memory.  x scales through L1;
+    // h scales from L2 (a split w2 item may meet a 128-byte line of them
+    // whose other groups another CTA writes later).
+    int si = 0;
+    uint32_t ph = 0;
     int cur_item = -1, cur_pass = -1;
     TcItem it{};
     TcSlot s{};
-    const float* ws0 = nullptr;  // weight-scale rows: A gate / up, B the 128-row block
+    const float* ws0 = nullptr;
     const float* ws1 = nullptr;
-    const float* xsr = nullptr;  // this lane's token's scale row (A: x, B: h), null past the pass
-    int out_row = 0;             // B: this lane's token's output row
-    uint32_t pe = 0;  // A-item pass ends so far: the amax buffer and barrier alternate with it
-    int si = 0;
-    uint32_t ph = 0;
+    const float* xsr[2] = {nullptr, nullptr};  // scale rows of this lane's columns lane, lane + 32
     while (true) {
-      if (!mbar_wait_t(tfull + si, ph, status)) break;
-      const int* tm = tmeta + kMetaInts * si;
-      const int4 m0 = *reinterpret_cast<const int4*>(tm);
-      const int4 m1 = *reinterpret_cast<const int4*>(tm + 4);
+      if (!mbar_wait_t(mready + si, ph, status)) break;
+      const int* md = meta + kMetaInts * si;
+      const int4 m0 = *reinterpret_cast<const int4*>(md);
+      const int4 m1 = *reinterpret_cast<const int4*>(md + 4);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty + si);  // the descriptor is read
       if (m0.w & kFEnd) break;
-      const int item = m0.x, pass = m0.y, kb = m0.z, fl = m0.w, ntok = m1.x, nkv = m1.z;
-      const bool a = (fl & kFA) != 0;
+      const int item = m0.x, pass = m0.y, kb = m0.z, ntok = m1.x, nkv = m1.z;
+      const bool a = (m0.w & kFA) != 0;
       if (item != cur_item) {
         cur_item = item;
         cur_pass = -1;
-        // routed items come after the producer loaded the routing tables
         const int n_act = *(volatile int*)(s_misc + 1);
-        const int totA = nA_sh + n_act * nA_r;
-        it = tc_decode(item, nA_sh, nA_r, totA, nB, q.sh_segs, has_shared);
+        it = tc_decode(item, nA_sh, nA_r, nA_sh + n_act * nA_r, nB, q, has_shared);
         s = tc_slot(p, s_off, s_act, it.slot, has_shared);
         if (it.a) {
           const float* base = s.e < 0 ? p.sw13_s : p.w13_s + (size_t)s.e * (2 * p.I / kBlock) * nkbH;
@@ -502,62 +550,121 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (pass != cur_pass) {
         cur_pass = pass;
-        const int tl = pass * kPass + col0 + lane;  // this lane's token of the slot
-        xsr = nullptr;
-        if (col0 + lane < ntok) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c = lane + 32 * h, tl = pass * kPass + c;
+          xsr[h] = nullptr;
+          if (c < ntok) {
+            if (a) {
+              const int tok = s.e < 0 ? tl : __ldcg(p.sorted + s.o + tl) / p.k;
+              xsr[h] = p.xs + (size_t)tok * nkbH;
+            } else {
+              xsr[h] = p.hs + (size_t)(s.hbase + tl) * p.hsS;
+            }
+          }
+        }
+      }
+      // the previous use of this stage's products has been read by the epilogue
+      if (!mbar_wait_t(tempty + si, ph ^ 1u, status)) break;
+      float* cs = cstage + si * 2 * kPass;
+      const float w0 = ld_ca(ws0 + kb);
+      const float w1 = a ? ld_ca(ws1 + kb) : (nkv > 1 ? ld_ca(ws0 + kb + 1) : 0.f);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int c = lane + 32 * h;
+        float c0 = 0.f, c1 = 0.f;
+        if (xsr[h]) {
           if (a) {
-            const int tok = s.e < 0 ? tl : __ldcg(p.sorted + s.o + tl) / p.k;
-            xsr = p.xs + (size_t)tok * nkbH;
+            const float sx = ld_ca(xsr[h] + kb);
+            c0 = w0 * sx;
+            c1 = w1 * sx;
           } else {
-            xsr = p.hs + (size_t)(s.hbase + tl) * p.hsS;
-            out_row = s.e < 0 ? tl : __ldcg(p.sorted + s.o + tl);
+            c0 = w0 * __ldcg(xsr[h] + kb);
+            c1 = nkv > 1 ? w1 * __ldcg(xsr[h] + kb + 1) : 0.f;
           }
         }
+        cs[c] = c0;
+        cs[kPass + c] = c1;
       }
-      const bool mine = col0 < ntok;  // this warp's columns hold tokens of the pass
-      if (mine) {
-        // scale of each column: weight block scale x token group scale (x
-        // scales through L1; h scales from L2, since a split w2 item may meet
-        // a line whose other groups another CTA writes later)
-        float c0, c1;
-        if (a) {
-          const float sx = xsr ? ld_ca(xsr + kb) : 0.f;
-          c0 = ld_ca(ws0 + kb) * sx;
-          c1 = ld_ca(ws1 + kb) * sx;
-        } else {
-          c0 = xsr ? ld_ca(ws0 + kb) * __ldcg(xsr + kb) : 0.f;
-          c1 = (xsr && nkv > 1) ? ld_ca(ws0 + kb + 1) * __ldcg(xsr + kb + 1) : 0.f;
-        }
-        cb[lane] = c0;
-        cb[32 + lane] = c1;
-        __syncwarp();
-      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(sready + si);
+      if (++si == kNST) { si = 0; ph ^= 1u; }
+    }
+  } else if (warp >= kEW0) {
+    // ================================================================ epilogue
+    // Warp (qd, hf) owns rows 32 qd .. 32 qd + 31 of the 128-row tile and the
+    // 16-column blocks hf and 2 + hf of a pass: accumulator index j < 16 is
+    // column 16 hf + j, j >= 16 column 32 + 16 hf + (j - 16), so that passes
+    // of up to 32 tokens still keep all eight warps busy.
+    const int ew = warp - kEW0;
+    const int qd = warp & 3;           // tensor-memory lane quadrant
+    const int hf = ew >> 2;
+    const int r = 32 * qd + lane;      // this thread's row of the 128-row tile
+    const int colA = 16 * hf, colB = 32 + 16 * hf;
+    const int my_col = lane < 16 ? colA + lane : colB + lane - 16;  // this lane's column (pass ends)
+    float acc0[32], acc1[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) acc0[j] = acc1[j] = 0.f;
+    int cur_item = -1;
+    TcItem it{};
+    TcSlot s{};
+    uint32_t pe = 0;  // A-item pass ends so far: the amax buffer and barrier alternate with it
+    uint32_t pu = 0;  // split w13 item ends so far (psync / pdec phases)
+    int si = 0;
+    uint32_t ph = 0;
+    while (true) {
+      if (!mbar_wait_t(tfull + si, ph, status)) break;
+      const int* tm = tmeta + kMetaInts * si;
+      const int4 m0 = *reinterpret_cast<const int4*>(tm);
+      const int4 m1 = *reinterpret_cast<const int4*>(tm + 4);
+      if (m0.w & kFEnd) break;
+      const int item = m0.x, pass = m0.y, fl = m0.w, ntok = m1.x, nkv = m1.z;
+      const bool a = (fl & kFA) != 0;
+      if (!mbar_wait_t(sready + si, ph, status)) break;
       tc_fence_after();
-      if (mine) {
-        const uint32_t ta = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(si * 2 * kPass + col0);
+      const bool blkA = colA < ntok, blkB = colB < ntok;  // (warp-uniform) blocks holding tokens
+      const bool two = a || nkv > 1;                      // the stage's second accumulator is live
+      if (blkA || blkB) {
+        const uint32_t ta = tmem + ((uint32_t)(32 * qd) << 16) + (uint32_t)(si * 2 * kPass);
+        const float* cs = cstage + si * 2 * kPass;
         float d[32];
-        tc_ld32(ta, d);
+        // the first accumulator of the stage (gate rows, or the first k-block)
+        if (blkA) tc_ld16(ta + colA, d);
+        if (blkB) tc_ld16(ta + colB, d + 16);
+        tc_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; j += 4) {
-          const float4 f0 = *reinterpret_cast<const float4*>(cb + j);
-          acc0[j] += d[j] * f0.x; acc0[j + 1] += d[j + 1] * f0.y;
-          acc0[j + 2] += d[j + 2] * f0.z; acc0[j + 3] += d[j + 3] * f0.w;
-        }
-        if (a) {
-          tc_ld32(ta + kPass, d);  // the up rows
+        for (int h = 0; h < 2; ++h) {
+          if (h == 0 ? !blkA : !blkB) continue;
+          const int col = h == 0 ? colA : colB;
 #pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            const float4 f1 = *reinterpret_cast<const float4*>(cb + 32 + j);
-            acc1[j] += d[j] * f1.x; acc1[j + 1] += d[j + 1] * f1.y;
-            acc1[j + 2] += d[j + 2] * f1.z; acc1[j + 3] += d[j + 3] * f1.w;
+          for (int j = 0; j < 16; j += 4) {
+            const float4 f0 = *reinterpret_cast<const float4*>(cs + col + j);
+            const int i = 16 * h + j;
+            acc0[i] += d[i] * f0.x; acc0[i + 1] += d[i + 1] * f0.y;
+            acc0[i + 2] += d[i + 2] * f0.z; acc0[i + 3] += d[i + 3] * f0.w;
           }
-        } else if (nkv > 1) {
-          tc_ld32(ta + kPass, d);  // the stage's second k-block
+        }
+        if (two) {
+          // the second: up rows (A) or the stage's second k-block (B)
+          if (blkA) tc_ld16(ta + kPass + colA, d);
+          if (blkB) tc_ld16(ta + kPass + colB, d + 16);
+          tc_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            const float4 f1 = *reinterpret_cast<const float4*>(cb + 32 + j);
-            acc0[j] += d[j] * f1.x; acc0[j + 1] += d[j + 1] * f1.y;
-            acc0[j + 2] += d[j + 2] * f1.z; acc0[j + 3] += d[j + 3] * f1.w;
+          for (int h = 0; h < 2; ++h) {
+            if (h == 0 ? !blkA : !blkB) continue;
+            const int col = h == 0 ? colA : colB;
+#pragma unroll
+            for (int j = 0; j < 16; j += 4) {
+              const float4 f1 = *reinterpret_cast<const float4*>(cs + kPass + col + j);
+              const int i = 16 * h + j;
+              if (a) {
+                acc1[i] += d[i] * f1.x; acc1[i + 1] += d[i + 1] * f1.y;
+                acc1[i + 2] += d[i + 2] * f1.z; acc1[i + 3] += d[i + 3] * f1.w;
+              } else {
+                acc0[i] += d[i] * f1.x; acc0[i + 1] += d[i + 1] * f1.y;
+                acc0[i + 2] += d[i + 2] * f1.z; acc0[i + 3] += d[i + 3] * f1.w;
+              }
+            }
           }
         }
       }
@@ -568,28 +675,92 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(fl & kFLast)) continue;
 
       // ---- end of a pass
-      const int nval = min(32, max(0, ntok - col0));  // this warp's token columns
-      const int tl0 = pass * kPass + col0;
+      if (item != cur_item) {
+        cur_item = item;
+        const int n_act = *(volatile int*)(s_misc + 1);
+        it = tc_decode(item, nA_sh, nA_r, nA_sh + n_act * nA_r, nB, q, has_shared);
+        s = tc_slot(p, s_off, s_act, it.slot, has_shared);
+      }
+      const int tl_me = pass * kPass + my_col;  // this lane's token of the slot (if my_col < ntok)
+      const int nA = min(16, max(0, ntok - colA)), nB = min(16, max(0, ntok - colB));  // tokens in each block
       if (!a) {
         // w2: this thread's row of every token's output (fp32), unweighted
         const int hrow = kRows * it.idx + r;
         float* base = s.e < 0 ? p.shared_out + (size_t)it.seg * p.M * p.H : p.rows;
+        const int out_row = my_col < ntok ? (s.e < 0 ? tl_me : __ldcg(p.sorted + s.o + tl_me)) : 0;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const int orow = __shfl_sync(0xffffffffu, out_row, j);
-          if (j < nval) base[(size_t)orow * p.H + hrow] = acc0[j];
+          if (j < 16 ? j < nA : j - 16 < nB) {
+            const int orow = __shfl_sync(0xffffffffu, out_row, j);
+            base[(size_t)orow * p.H + hrow] = acc0[j];
+          }
         }
       } else {
-        // w13: h = silu(min(g, L)) * clamp(u, -L, L), then FP8 per token over the
-        // 128 intermediates of this item (the four lane quadrants of the column half)
+        const int grp = it.idx;  // the item's 128 intermediates are h group idx
+        if (s.e < 0 && q.a_segs > 1) {
+          // a K segment of a split w13 item: its partial [g; u] rows go to the
+          // workspace; the item that completes the group adds every segment's
+          // rows in segment order and goes on below, the others are done
+          const size_t gbase = (size_t)grp * q.a_segs * 2 * kPass * kRows;
+          float* part = q.gu_part + gbase + (size_t)it.seg * 2 * kPass * kRows;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = j < 16 ? colA + j : colB + j - 16;
+            if (col < ntok) {
+              part[(size_t)col * kRows + r] = acc0[j];
+              part[(size_t)(kPass + col) * kRows + r] = acc1[j];
+            }
+          }
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(psync);
+          if (!mbar_wait_t(psync, pu & 1u, status)) break;
+          if (ew == 0 && lane == 0) {
+            __threadfence();
+            const int last = atomicAdd(q.pcount + grp, 1) == q.a_segs - 1;
+            s_misc[2] = last;
+            if (!last) atomicAdd(p.hdr + kHdrDoneA, 1);  // (the completing item counts when it publishes)
+            mbar_arrive(pdec);
+          }
+          const bool ok = mbar_wait_t(pdec, pu & 1u, status);
+          ++pu;
+          if (!ok) break;
+          if (!*(volatile int*)(s_misc + 2)) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc0[j] = acc1[j] = 0.f;
+            continue;
+          }
+          __threadfence();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int col = j < 16 ? colA + j : colB + j - 16;
+            float g = 0.f, u = 0.f;
+            if (col < ntok)
+              for (int sg = 0; sg < q.a_segs; ++sg) {
+                const float* ps = q.gu_part + gbase + (size_t)sg * 2 * kPass * kRows;
+                g += __ldcg(ps + (size_t)col * kRows + r);
+                u += __ldcg(ps + (size_t)(kPass + col) * kRows + r);
+              }
+            acc0[j] = g;
+            acc1[j] = u;
+          }
+        }
+        // w13: h = silu(min(g, L)) * clamp(u, -L, L) for the columns that hold
+        // tokens (the counts are the same in the whole warp), then FP8 per token
+        // over the 128 intermediates of this item (the four lane quadrants of
+        // the column half)
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float z = fminf(acc0[j], p.limit);
-          acc0[j] = z / (1.f + expf(-z)) * fminf(fmaxf(acc1[j], -p.limit), p.limit);
-          acc1[j] = j < nval ? fabsf(acc0[j]) : 0.f;
+          if (j < 16 ? j < nA : j - 16 < nB) {
+            const float z = fminf(acc0[j], p.limit);
+            acc0[j] = __fdividef(z, 1.f + __expf(-z)) * fminf(fmaxf(acc1[j], -p.limit), p.limit);
+            acc1[j] = fabsf(acc0[j]);
+          } else {
+            acc1[j] = 0.f;
+          }
         }
         // per-column max over this warp's 32 rows: after the five exchange
-        // steps lane l holds the max of column l
+        // steps lane l holds the max of accumulator column l
 #pragma unroll
         for (int sh = 16; sh >= 1; sh >>= 1) {
           const bool upper = (lane & sh) != 0;
@@ -610,18 +781,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         const float amax = fmaxf(fmaxf(ab[lane], ab[32 + lane]), fmaxf(ab[64 + lane], ab[96 + lane]));
         const float scl = group_scale(amax, p.e8m0 != 0);
-        const int grp = it.idx;  // the item's 128 intermediates are h group idx
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float sj = __shfl_sync(0xffffffffu, scl, j);
-          if (j < nval) {
-            const size_t row = (size_t)(s.hbase + tl0 + j);
+          if (j < 16 ? j < nA : j - 16 < nB) {
+            const int col = j < 16 ? colA + j : colB + j - 16;
+            const float sj = __shfl_sync(0xffffffffu, scl, j);
+            const size_t row = (size_t)(s.hbase + pass * kPass + col);
             uint16_t code;
             asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(code) : "f"(0.f), "f"(__fdiv_rn(acc0[j], sj)));
             p.hq[row * p.Imax + grp * kBlock + r] = (uint8_t)(code & 0xff);
           }
         }
-        if (qd == 0 && lane < nval) p.hs[(size_t)(s.hbase + tl0 + lane) * p.hsS + grp] = scl;
+        if (qd == 0 && my_col < ntok) p.hs[(size_t)(s.hbase + tl_me) * p.hsS + grp] = scl;
         if (fl & kFFinal) {
           // this warp's part of the group is written: publish it (the codes are
           // read with TMA by other CTAs); the eighth warp counts the item
@@ -673,45 +844,69 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint8_t* xq, con
   }
 }
 
-size_t tc_smem_bytes(int E) {
-  return 1024 + (size_t)kNST * kSlotB + 2 * kNST * kMetaInts * sizeof(int) +
-         (4 * kNST + 4 + 2) * sizeof(uint64_t) + (kNEpi * 64 + 2 * 2 * 4 * 32) * sizeof(float) +
-         (4 + 2 * E + 1) * sizeof(int);
-}
+size_t tc_smem_bytes(int E) { return SmemTc::bytes(E); }
 
 }  // namespace
 
-int tc_shared_segments(int Is, int M) {
-  // a dense layer's long w2 rows (I_s / 128 k-blocks) are split into segments
-  // of 16 k-blocks while one pass holds all tokens, so that the w2 phase has
-  // enough items for every SM; the boundary adds the partial rows
-  if (Is <= 0 || M > kPass) return 1;
-  return std::max(1, (Is / kBlock + kSegKB - 1) / kSegKB);
+int tc_w13_segments(int E, int H, int Is, int M) {
+  // a dense layer's w13 items (one per 128 intermediates: fewer than a wave
+  // of SMs can balance) are split four ways over H while one pass holds all
+  // tokens, so that groups complete in several waves and the w2 items start
+  // behind them; the completing segment adds the partial rows
+  return (E == 0 && Is > 0 && M <= kPass) ? std::min(kW13Segs, H / kBlock) : 1;
 }
 
-cudaError_t launch_experts_tc(const ExpertArgs& a, const uint8_t* xg, int sh_segs, int num_sms, cudaStream_t s) {
+size_t tc_w13_partial_bytes(int E, int Is) {
+  return E == 0 && Is > 0 && kW13Segs > 1 ? (size_t)(Is / kBlock) * kW13Segs * 2 * kPass * kRows * sizeof(float) : 0;
+}
+
+int tc_shared_segments(int H, int Is, int M, int num_sms) {
+  // a dense layer's long w2 rows (I_s / 128 k-blocks) are split into K
+  // segments while one pass holds all tokens: as many as make about three
+  // equal items per SM (the w2 phase runs as whole waves), at most one per
+  // k-block; the boundary adds the partial rows
+  if (Is <= 0 || M > kPass) return 1;
+  const int nB = H / kRows;
+  return std::max(1, std::min({Is / kBlock, kMaxSharedSegs, (kSegWaves * num_sms + nB / 2) / nB}));
+}
+
+static_assert(sizeof(TcMaps) <= sizeof(ExpertsLaunch::maps), "tensor maps fit the prepared launch");
+
+cudaError_t prepare_experts_tc(const ExpertArgs& a, const TcExtra& x, ExpertsLaunch& L) {
   if (!encode_fn()) return cudaErrorNotSupported;
-  TcMaps maps;
-  memset(&maps, 0, sizeof(maps));
+  memset(&L, 0, sizeof(L));
+  L.a = a;
+  L.tc = true;
+  L.tcx = x;
+  const uint8_t* xg = x.xg;
+  TcMaps* maps = reinterpret_cast<TcMaps*>(L.maps);
   // weights: [rows][K] bytes, box one k-block x 128 rows; activations box one k-block x 16 rows
-  if (a.E > 0 && (!tmap_2d(&maps.w13, a.w13, a.H, (uint64_t)a.E * 2 * a.I, 128, kRows) ||
-                  !tmap_2d(&maps.w2, a.w2, a.I, (uint64_t)a.E * a.H, 128, kRows) ||
-                  !tmap_2d(&maps.xg, xg, a.H, a.Mk, 128, 16)))
+  if (a.E > 0 && (!tmap_2d(&maps->w13, a.w13, a.H, (uint64_t)a.E * 2 * a.I, 128, kRows) ||
+                  !tmap_2d(&maps->w2, a.w2, a.I, (uint64_t)a.E * a.H, 128, kRows) ||
+                  !tmap_2d(&maps->xg, xg, a.H, a.Mk, 128, 16)))
     return cudaErrorInvalidValue;
-  if (a.Is > 0 && (!tmap_2d(&maps.sw13, a.sw13, a.H, 2 * (uint64_t)a.Is, 128, kRows) ||
-                   !tmap_2d(&maps.sw2, a.sw2, a.Is, a.H, 128, kRows)))
+  if (a.Is > 0 && (!tmap_2d(&maps->sw13, a.sw13, a.H, 2 * (uint64_t)a.Is, 128, kRows) ||
+                   !tmap_2d(&maps->sw2, a.sw2, a.Is, a.H, 128, kRows)))
     return cudaErrorInvalidValue;
-  if (!tmap_2d(&maps.xq, a.xq, a.H, a.M, 128, 16) || !tmap_2d(&maps.hq, a.hq, a.Imax, (uint64_t)a.Mk + a.M, 128, 16))
+  if (!tmap_2d(&maps->xq, a.xq, a.H, a.M, 128, 16) ||
+      !tmap_2d(&maps->hq, a.hq, a.Imax, (uint64_t)a.Mk + a.M, 128, 16))
     return cudaErrorInvalidValue;
-  const size_t smem = tc_smem_bytes(a.E);
-  if (smem > 227 * 1024) return cudaErrorInvalidConfiguration;
-  cudaError_t err = cudaFuncSetAttribute(experts_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (err != cudaSuccess) return err;
+  L.smem = tc_smem_bytes(a.E);
+  if (L.smem > 227 * 1024) return cudaErrorInvalidConfiguration;
+  return cudaFuncSetAttribute(experts_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem);
+}
+
+cudaError_t launch_experts_tc_prepared(const ExpertsLaunch& L, int num_sms, cudaStream_t s) {
+  TcMaps maps;
+  memcpy(&maps, L.maps, sizeof(maps));
   TcArgs q;
-  q.xg = xg;
-  q.sh_segs = sh_segs;
-  PdlLaunch L(dim3(num_sms), dim3(kThreads), smem, s);
-  return cudaLaunchKernelEx(&L.cfg, experts_tc_kernel, a, q, maps);
+  q.xg = L.tcx.xg;
+  q.sh_segs = L.tcx.sh_segs;
+  q.a_segs = L.tcx.a_segs;
+  q.gu_part = L.tcx.gu_part;
+  q.pcount = L.tcx.pcount;
+  PdlLaunch P(dim3(num_sms), dim3(kThreads), L.smem, s);
+  return cudaLaunchKernelEx(&P.cfg, experts_tc_kernel, L.a, q, maps);
 }
 
 cudaError_t launch_gather_rows(const uint8_t* xq, const int* sorted, int k, int Mk, int H, uint8_t* xg, int num_sms,

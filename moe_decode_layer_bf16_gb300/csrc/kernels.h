@@ -1,6 +1,7 @@
 // Internal launch interfaces between the C ABI (api.cu) and the kernels.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -116,16 +117,42 @@ struct ExpertArgs {
   int router_ctas;  // CTAs of the router launch that precedes this kernel
   int bq;           // w2 item size in 32-row quarters of a 128-row block: 4, or 1 for long rows
 };
-cudaError_t launch_experts(const ExpertArgs& a, int num_sms, cudaStream_t s);
-
-// The tensor-core (tcgen05) form of the expert kernel for wide passes: xg
-// holds the routed tokens' x codes in route order (written by
-// launch_gather_rows), sh_segs the K segments of the shared slot's w2 items
-// (tc_shared_segments), whose partial rows follow one another in shared_out.
-cudaError_t launch_experts_tc(const ExpertArgs& a, const uint8_t* xg, int sh_segs, int num_sms, cudaStream_t s);
+// An expert-kernel launch prepared on the host (tensor maps encoded, the
+// pass width and ring depth chosen, the shared-memory limit set) before the
+// router is enqueued, so that no host work falls between the router's and the
+// expert kernel's launches.
+// Extra arguments of the tensor-core (tcgen05) form of the expert kernel:
+//   xg       the routed tokens' x codes in route order (launch_gather_rows)
+//   sh_segs  K segments of the shared slot's w2 items (tc_shared_segments),
+//            whose partial rows follow one another in shared_out
+//   a_segs   K segments of the shared slot's w13 items (tc_w13_segments),
+//            partial [g; u] rows in gu_part (tc_w13_partial_bytes), counted
+//            per group in pcount (zeroed by the router with the counters)
+struct TcExtra {
+  const uint8_t* xg;
+  int sh_segs;
+  int a_segs;
+  float* gu_part;
+  int* pcount;
+};
+struct ExpertsLaunch {
+  ExpertArgs a;
+  CUtensorMap maps[7];
+  bool tc;               // the tcgen05 kernel (else the warp-MMA kernel)
+  int tt;                // warp-MMA kernel: 8-token columns per pass
+  int nst;               // warp-MMA kernel: ring stages
+  size_t smem;           // dynamic shared memory
+  TcExtra tcx;           // tcgen05 kernel
+};
+cudaError_t prepare_experts(const ExpertArgs& a, ExpertsLaunch& L);
+cudaError_t prepare_experts_tc(const ExpertArgs& a, const TcExtra& x, ExpertsLaunch& L);
+cudaError_t launch_experts(const ExpertsLaunch& L, int num_sms, cudaStream_t s);
 cudaError_t launch_gather_rows(const uint8_t* xq, const int* sorted, int k, int Mk, int H, uint8_t* xg, int num_sms,
                                cudaStream_t s);
-int tc_shared_segments(int Is, int M);
+constexpr int kMaxSharedSegs = 16;  // K segments of a dense layer's w2 items at most
+int tc_shared_segments(int H, int Is, int M, int num_sms);
+int tc_w13_segments(int E, int H, int Is, int M);
+size_t tc_w13_partial_bytes(int E, int Is);
 
 struct NormArgs {
   const void* x; const void* residual; const void* gain;

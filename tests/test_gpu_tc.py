@@ -1,8 +1,8 @@
 """The tensor-core (tcgen05) expert kernel against the CPU oracle, through the
 C ABI.  moe_set_expert_path forces the kernel, so that the same shapes the
 warp-MMA kernel is tested on run here too; the automatic choice is checked to
-pick this kernel where it is meant to run (dense layers above 8 tokens, MoE
-layers from 64 tokens).  Same bar as tests/test_gpu_parity.py: routing exact,
+pick this kernel where it is meant to run (dense layers from 4 tokens, MoE
+layers from 16 tokens).  Same bar as tests/test_gpu_parity.py: routing exact,
 weights within 1e-5, bf16 outputs within max-abs-rel 2e-2."""
 
 import numpy as np
@@ -99,6 +99,20 @@ def test_dense_layer_tiny_tc(tc_path, M):
     assert orc.max_abs_rel(g["residual_out"], ref["residual_out"]) <= TOL
 
 
+# a dense layer's w13 items are split over H: four segments of 1-2 k-blocks at
+# H = 640 (5 k-blocks), two at H = 256; the w2 items over I_s
+@pytest.mark.parametrize("hidden", [256, 640])
+@pytest.mark.parametrize("M", [1, 7, 33])
+def test_dense_layer_split_segments_tc(tc_path, hidden, M):
+    dims = TINY_DENSE.with_(hidden=hidden, shared_inter=2560)
+    lw = synth.make_layer(dims, seed=13, device=DEV)
+    x, res = synth.make_tokens(M, dims.hidden, seed=210 + M, device=DEV)
+    g = run_gpu(dims, lw, x, res)
+    ref = orc.moe_decode_layer(oracle_layer(dims, lw), to_np(x), to_np(res))
+    assert orc.max_abs_rel(g["out"], ref["out"]) <= TOL
+    assert orc.max_abs_rel(g["residual_out"], ref["residual_out"]) <= TOL
+
+
 # ------------------------------------------------------------ full size, automatic choice
 
 @pytest.fixture(scope="module")
@@ -109,8 +123,8 @@ def dsv3():
 
 @pytest.mark.parametrize("M", [9, 32, 64, 130])
 def test_dense_layer_dsv3_tc(M):
-    # DeepSeek-V3's dense MLP: above 8 tokens the automatic choice is the
-    # tcgen05 kernel; at 9-64 tokens its w2 items are split into 9 K segments
+    # DeepSeek-V3's dense MLP: from 4 tokens the automatic choice is the
+    # tcgen05 kernel; up to 64 tokens its w2 items are split into K segments
     # (partial rows the boundary adds), at 130 tokens three passes
     assert m.moe_decode_layer_plan(DSV3_DENSE, M) == (m.MOE_PATH_TCGEN05, 3)
     lw = synth.make_layer(DSV3_DENSE, seed=12, device=DEV)
