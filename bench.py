@@ -61,12 +61,18 @@ WORKLOAD = "deepseek-v3-shaped MoE decode layer, H=7168 E=256 k=8 I=Is=2048, M i
 EXPERT_BYTES = 2 * DSV3.inter * DSV3.hidden + DSV3.hidden * DSV3.inter + 4 * (
     (2 * DSV3.inter // 128) * (DSV3.hidden // 128) + (DSV3.hidden // 128) * (DSV3.inter // 128))
 ROUTER_BYTES = DSV3.num_experts * DSV3.hidden * 2
-# DRAM bytes (read + write) per activated expert of one expert-kernel launch, from an
-# ncu capture (profiles/experts_kernel_dsv3_e32_m8.txt) of the kernel built from the
-# experts.cu whose code (comments and white space removed) has the SHA-256 given; the
-# bench reports no traffic for any other code.
-TRAFFIC_CAPTURE = {"experts_cu_code_sha256": "5ede96a0a133b37727ac40d3395cb3e88334ceeb2180e08bea748a0ef0e6fcc8",
-                   "bytes_per_expert": 1_283_990_312 / 29}
+# DRAM bytes (read + write) per activated expert of one launch of each expert
+# kernel, from the ncu capture of profiles/experts_kernels_dsv3_e32_traffic.txt
+# (the 32-expert profiling layer: experts_kernel at 8 tokens, 29 experts active,
+# experts_tc_kernel at 32 tokens, 33 experts active), valid for the source whose
+# code (comments and white space removed) has the SHA-256 given; the bench
+# reports no traffic once a kernel's code differs from the captured one.
+TRAFFIC_CAPTURE = {
+    "experts.cu": {"code_sha256": "3e9ac52f224661882f0b3ee329d0db2e871ad28605b87bcef2683c0c7b5d4041",
+                   "bytes_per_expert": 44_169_575},
+    "experts_tc.cu": {"code_sha256": "0513010fb4821d17177604fa276254241b5d02755c2e3798dc9f5a0fecd111fa",
+                      "bytes_per_expert": 44_371_638},
+}
 
 
 def code_sha256(path):
@@ -653,11 +659,14 @@ def run_ours(args, world, rank, local):
 
     peak, peak_kind = load_peaks()
     achieved = exp_bytes_all / (exp_ms_all / 1e3) / 1e9
+    # which expert kernel each M runs (the library's choice)
+    kern = {M: "experts_tc.cu" if m.moe_decode_layer_plan(dims, M)[0] == m.MOE_PATH_TCGEN05 else "experts.cu"
+            for M in MS}
     traffic = None
-    src = os.path.join(ROOT, "moe_decode_layer_bf16_gb300", "csrc", "experts.cu")
-    if code_sha256(src) == TRAFFIC_CAPTURE["experts_cu_code_sha256"]:
+    csrc = os.path.join(ROOT, "moe_decode_layer_bf16_gb300", "csrc")
+    if all(code_sha256(os.path.join(csrc, f)) == c["code_sha256"] for f, c in TRAFFIC_CAPTURE.items()):
         # per launch, averaged over the launches like `achieved`
-        traffic = round(TRAFFIC_CAPTURE["bytes_per_expert"] * sum(unique[M] + 1 for M in MS) / len(MS))
+        traffic = round(sum(TRAFFIC_CAPTURE[kern[M]]["bytes_per_expert"] * (unique[M] + 1) for M in MS) / len(MS))
     for M in MS:
         per_m[str(M)]["frac_of_8TBs"] = round(per_m[str(M)]["layer_gbps"] / 8000.0, 3)
         per_m[str(M)]["frac_of_measured"] = round(per_m[str(M)]["layer_gbps"] / peak, 3)
@@ -752,7 +761,11 @@ def run_ours(args, world, rank, local):
                    "weights": "fp8-e4m3 with fp32 128x128 block scales; router bf16; activations bf16 in/out",
                    "parallelism": "replicas" if world > 1 else "single GPU", "per_m": per_m,
                    "wall_s_timed": round(wall, 4)},
-        "roofline": {"bound": "hbm", "kernel": "experts_kernel", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm",
+                     "kernel": "expert kernels: " + ", ".join(
+                         f"{'experts_tc_kernel' if kern[M] == 'experts_tc.cu' else 'experts_kernel'} at M={M}"
+                         for M in MS),
+                     "achieved": round(achieved, 1),
                      "peak": peak, "peak_kind": f"{peak_kind} HBM copy bandwidth", "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": round(exp_bytes_all / (len(MS) * args.steps))},

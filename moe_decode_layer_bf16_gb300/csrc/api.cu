@@ -283,7 +283,9 @@ static int layer_impl(const moe_layer_dims* dims, const moe_layer_weights* w, in
   // enqueued, so that no host work delays the expert kernel behind it
   const bool tc = expert_path(*dims, M) == MOE_PATH_TCGEN05;
   uint8_t* xg = ws + L.xg;
-  const int parts = tc ? tc_shared_segments(H, dims->shared_inter, M, sms) : 1;
+  const int parts = tc ? tc_shared_segments(E, H, dims->shared_inter, M, sms) : 1;
+  // the partial rows of split w2 items must fit the shared-output region
+  if ((size_t)parts * M > shared_rows(*dims, M)) return MOE_ERR_UNSUPPORTED;
   TcExtra tx;
   tx.xg = xg;
   tx.sh_segs = parts;

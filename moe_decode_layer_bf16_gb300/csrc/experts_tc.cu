@@ -860,12 +860,13 @@ size_t tc_w13_partial_bytes(int E, int Is) {
   return E == 0 && Is > 0 && kW13Segs > 1 ? (size_t)(Is / kBlock) * kW13Segs * 2 * kPass * kRows * sizeof(float) : 0;
 }
 
-int tc_shared_segments(int H, int Is, int M, int num_sms) {
+int tc_shared_segments(int E, int H, int Is, int M, int num_sms) {
   // a dense layer's long w2 rows (I_s / 128 k-blocks) are split into K
   // segments while one pass holds all tokens: as many as make about three
   // equal items per SM (the w2 phase runs as whole waves), at most one per
-  // k-block; the boundary adds the partial rows
-  if (Is <= 0 || M > kPass) return 1;
+  // k-block; the boundary adds the partial rows.  An MoE layer's shared
+  // expert is one of many experts and is never split.
+  if (E != 0 || Is <= 0 || M > kPass) return 1;
   const int nB = H / kRows;
   return std::max(1, std::min({Is / kBlock, kMaxSharedSegs, (kSegWaves * num_sms + nB / 2) / nB}));
 }

@@ -150,7 +150,7 @@ cudaError_t launch_experts(const ExpertsLaunch& L, int num_sms, cudaStream_t s);
 cudaError_t launch_gather_rows(const uint8_t* xq, const int* sorted, int k, int Mk, int H, uint8_t* xg, int num_sms,
                                cudaStream_t s);
 constexpr int kMaxSharedSegs = 16;  // K segments of a dense layer's w2 items at most
-int tc_shared_segments(int H, int Is, int M, int num_sms);
+int tc_shared_segments(int E, int H, int Is, int M, int num_sms);
 int tc_w13_segments(int E, int H, int Is, int M);
 size_t tc_w13_partial_bytes(int E, int Is);
 
