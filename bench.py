@@ -502,6 +502,42 @@ def dense_layer(m, flush_l2, dev, MS, reps=5):
     return res
 
 
+def tp_rank_partial(m, dims, lw, Ms, flush_l2, dev, peak, Gs=(2, 4, 8), reps=5):
+    """One rank's share of the layer under G-way tensor parallelism over each
+    expert's intermediate dimension (rank 0's shard through
+    moe_decode_layer_partial), and the boundary over G shares.  The all-reduce
+    between GPUs is not part of it (one GPU)."""
+    from moe_decode_layer_bf16_gb300 import tp
+    res = {}
+    for G in Gs:
+        sd = tp.shard_dims(dims, G)
+        shard = tp.shard_weights(dims, lw, 0, G)
+        ws = torch.empty(m.moe_decode_workspace_size(sd, max(Ms)), dtype=torch.uint8, device=dev)
+        m.moe_workspace_init(ws)
+        per = {}
+        for M in Ms:
+            x, r = synth.make_tokens(M, dims.hidden, seed=700 + M, device=dev)
+            mo = torch.empty((M, dims.hidden), dtype=torch.float32, device=dev)
+            ids = torch.empty((M, dims.top_k), dtype=torch.int32, device=dev)
+            us = 1e3 * statistics.median(
+                timed(lambda: m.moe_decode_layer_partial(sd, shard, x, mo, ws, topk_ids=ids), flush_l2, reps))
+            if m.moe_device_status(ws) != m.MOE_OK:
+                raise RuntimeError("tp partial status")
+            unique = int(torch.unique(ids).numel())
+            nbytes = (unique + 1) * EXPERT_BYTES / G + ROUTER_BYTES + M * dims.hidden * (2 + 4)
+            parts = torch.zeros((G, M, dims.hidden), dtype=torch.float32, device=dev)
+            o, ro = torch.empty_like(x), torch.empty_like(r)
+            ub = 1e3 * statistics.median(
+                timed(lambda: m.moe_tp_boundary(parts, r, lw["gain"], o, ro, dims.rms_eps), flush_l2, reps))
+            per[str(M)] = {"us_rank": round(us, 2), "rank_gbps": round(nbytes / us / 1e3, 1),
+                           "rank_frac_of_measured": round(nbytes / us / 1e3 / peak, 3),
+                           "us_boundary_over_G_shares": round(ub, 2)}
+        res[f"G={G}"] = per
+        del shard, ws
+        torch.cuda.empty_cache()
+    return res
+
+
 def graph_chain(m, dims, lw0, MS, n_layers, reps, dev):
     """A decode chain captured as one CUDA graph: n_layers layers with distinct
     weights, each layer's out / residual_out feeding the next layer's x /
@@ -725,6 +761,12 @@ def run_ours(args, world, rank, local):
                 "[M,7168] x [256,7168]^T -> fp32 logits (3.67 MB: launch-bound, its fraction of the HBM "
                 "roofline is not meaningful), L2 flushed, median of 5",
                 lambda: splitk_proj(m, flush_l2, dev, 256, 7168, fp32=True))
+        if dims.num_experts == DSV3.num_experts:
+            attempt("tp_rank_partial", "G-way tensor parallelism over each expert's intermediate dimension: one "
+                    "rank's share of the layer (moe_decode_layer_partial on rank 0's shard, 1/G of every expert's "
+                    "bytes) and the boundary over G shares (moe_tp_boundary); the all-reduce between GPUs is not "
+                    "measured (one GPU), L2 flushed, median of 5",
+                    lambda: tp_rank_partial(m, dims, lw, MS, flush_l2, dev, peak))
         attempt("graph_chain", "3 layers with distinct weights captured as one CUDA graph, each layer's outputs "
                 "feeding the next, replayed back to back without L2 flushes",
                 lambda: graph_chain(m, dims, lw, MS, 3, 10, dev))

@@ -172,6 +172,37 @@ int moe_decode_layer_traced(const moe_layer_dims *dims, const moe_layer_weights 
                             int32_t *expert_offsets, void *workspace, size_t ws_bytes,
                             void *stream, void *const *events);
 
+/*
+ * Tensor parallelism over each expert's intermediate dimension ([decode page]
+ * LayerStages leaves the MoE sublayer "TP-partial"; [draft page] module
+ * docstring: the boundaries fuse the all-reduce with the residual add and the
+ * RMSNorm).  Rank g of G holds, of every routed expert and of the shared
+ * expert, the gate rows [g I/G, (g+1) I/G) and the same up rows of w13, and the
+ * same columns of w2, with their block scales (I/G and I_s/G multiples of 128,
+ * so that no 128 x 128 scale block and no h quantisation group straddles two
+ * ranks).  A rank's shard is therefore an MoE layer with inter = I/G and
+ * shared_inter = I_s/G (router weight and bias replicated), and:
+ *
+ * moe_decode_layer_partial: moe_decode_layer on a rank's shard up to the
+ *   weighted finalize: m_out (fp32 [M, H]) = sum_j w_j * y_(t,j) + y_shared,
+ *   this rank's share of m; the ranks' m_out sum to the whole layer's m.  No
+ *   residual, gain or bf16 outputs (norm_gain may be NULL).  Same workspace
+ *   and routing outputs as moe_decode_layer; launches its kernels alike (the
+ *   boundary kernel writes m_out instead of normalising).
+ *
+ * moe_tp_boundary: the layer boundary over G partial sums in this GPU's
+ *   memory (gathered by the caller, e.g. an all-gather or peer copies):
+ *   m = sum_{g < G} partials[g] (in rank order, fp32), r' = m + residual,
+ *   residual_out = bf16(r'), out = bf16(bf16(r') * rsqrt(mean(bf16(r')^2) +
+ *   eps) * gain).  partials fp32 [G, M, H]; the rest as rmsnorm_residual.
+ */
+int moe_decode_layer_partial(const moe_layer_dims *dims, const moe_layer_weights *w, int M,
+                             const void *x, float *m_out, int32_t *topk_ids, float *topk_w,
+                             int32_t *sorted_routes, int32_t *expert_offsets, void *workspace,
+                             size_t ws_bytes, void *stream);
+int moe_tp_boundary(const float *partials, int G, const void *residual, const void *gain, int M, int H,
+                    float eps, void *out, void *residual_out, void *stream);
+
 /* Bytes of workspace splitk_gemm_bf16 needs for this shape and split_k. */
 int splitk_gemm_workspace_size(int M, int N, int K, int split_k, size_t *bytes);
 

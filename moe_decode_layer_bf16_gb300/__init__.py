@@ -73,6 +73,9 @@ def lib() -> ctypes.CDLL:
         L.moe_decode_layer.argtypes = [ctypes.POINTER(_Dims), ctypes.POINTER(_Weights), _i, _vp, _vp, _vp,
                                        _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
         L.moe_decode_layer_traced.argtypes = L.moe_decode_layer.argtypes + [ctypes.POINTER(_vp)]
+        L.moe_decode_layer_partial.argtypes = [ctypes.POINTER(_Dims), ctypes.POINTER(_Weights), _i, _vp, _vp,
+                                               _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+        L.moe_tp_boundary.argtypes = [_vp, _i, _vp, _vp, _i, _i, _f, _vp, _vp, _vp]
         L.splitk_gemm_workspace_size.argtypes = [_i, _i, _i, _i, ctypes.POINTER(_sz)]
         L.splitk_gemm_bf16.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _sz, _vp]
         L.splitk_gemm_bf16_noalloc.argtypes = [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp]
@@ -89,7 +92,7 @@ def lib() -> ctypes.CDLL:
         for n in ("moe_decode_workspace_size", "moe_workspace_init", "moe_decode_layer", "moe_decode_layer_traced",
                   "splitk_gemm_workspace_size", "splitk_gemm_bf16", "splitk_gemm_bf16_noalloc", "rmsnorm_residual",
                   "moe_device_status", "moe_debug_set_fault", "moe_debug_fill_noalloc_scratch",
-                  "moe_decode_layer_plan", "moe_set_expert_path",
+                  "moe_decode_layer_plan", "moe_set_expert_path", "moe_decode_layer_partial", "moe_tp_boundary",
                   "mtp_eh_front_workspace_size", "mtp_eh_front"):
             getattr(L, n).restype = ctypes.c_int
         _lib = L
@@ -172,6 +175,28 @@ def moe_decode_layer_traced(dims: LayerDims, weights: dict, x, residual, out, re
                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
                                        _stream(stream), ev)
     _check(rc, "moe_decode_layer_traced")
+
+
+def moe_decode_layer_partial(dims: LayerDims, weights: dict, x, m_out, workspace, topk_ids=None, topk_w=None,
+                             sorted_routes=None, expert_offsets=None, stream=None):
+    """A tensor-parallel rank's share of the layer (see include/moe_decode.h):
+    m_out (float32 [M, H]) = the weighted finalize of this rank's shard."""
+    w = _Weights(*[_ptr(weights.get(n, weights.get("gain") if n == "norm_gain" else None))
+                   for n in _WEIGHT_FIELDS])
+    rc = lib().moe_decode_layer_partial(ctypes.byref(_dims(dims)), ctypes.byref(w), int(x.shape[0]), _ptr(x),
+                                        _ptr(m_out), _ptr(topk_ids), _ptr(topk_w), _ptr(sorted_routes),
+                                        _ptr(expert_offsets), _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _stream(stream))
+    _check(rc, "moe_decode_layer_partial")
+
+
+def moe_tp_boundary(partials, residual, gain, out, residual_out, eps: float, stream=None):
+    """The boundary over G partial sums (float32 [G, M, H]): their sum plus the
+    residual, then RMSNorm with the gain."""
+    G, M, H = partials.shape
+    rc = lib().moe_tp_boundary(_ptr(partials), int(G), _ptr(residual), _ptr(gain), int(M), int(H), float(eps),
+                               _ptr(out), _ptr(residual_out), _stream(stream))
+    _check(rc, "moe_tp_boundary")
 
 
 def splitk_gemm_workspace_size(M: int, N: int, K: int, split_k: int = 0) -> int:

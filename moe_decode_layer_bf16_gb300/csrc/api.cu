@@ -201,7 +201,7 @@ int moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
 static int layer_impl(const moe_layer_dims* dims, const moe_layer_weights* w, int M, const void* x,
                       const void* residual, void* out, void* residual_out, int32_t* topk_ids,
                       float* topk_w, int32_t* sorted_routes, int32_t* expert_offsets, void* workspace,
-                      size_t ws_bytes, void* stream, void* const* events) {
+                      size_t ws_bytes, void* stream, void* const* events, float* m_out = nullptr) {
   int rc = check_dims(dims);
   if (rc != MOE_OK) return rc;
   if (!w || M < 0) return MOE_ERR_INVALID_ARG;
@@ -210,12 +210,14 @@ static int layer_impl(const moe_layer_dims* dims, const moe_layer_weights* w, in
   const bool has_shared = dims->shared_inter > 0;
   const bool dense = dims->num_experts == 0;  // routed weights are not read (may be NULL)
   if (!dense && (!w->router_w || !w->w13 || !w->w13_s || !w->w2 || !w->w2_s)) return MOE_ERR_INVALID_ARG;
-  if (!w->norm_gain) return MOE_ERR_INVALID_ARG;
+  const bool partial = m_out != nullptr;  // a rank's partial sum: no residual, gain or outputs
+  if (!partial && !w->norm_gain) return MOE_ERR_INVALID_ARG;
   if (has_shared && (!w->sw13 || !w->sw13_s || !w->sw2 || !w->sw2_s)) return MOE_ERR_INVALID_ARG;
-  if (!x || !residual || !out || !residual_out || !workspace) return MOE_ERR_INVALID_ARG;
+  if (!x || !workspace || (!partial && (!residual || !out || !residual_out))) return MOE_ERR_INVALID_ARG;
   if ((!dense && (!aligned16(w->router_w) || !aligned16(w->w13) || !aligned16(w->w2))) || !aligned16(x) ||
-      !aligned16(residual) || !aligned16(out) || !aligned16(residual_out) || !aligned16(w->norm_gain) ||
-      !aligned16(workspace) || (has_shared && (!aligned16(w->sw13) || !aligned16(w->sw2))))
+      !aligned16(workspace) || (has_shared && (!aligned16(w->sw13) || !aligned16(w->sw2))) ||
+      (partial ? !aligned16(m_out)
+               : (!aligned16(residual) || !aligned16(out) || !aligned16(residual_out) || !aligned16(w->norm_gain))))
     return MOE_ERR_INVALID_ARG;
   Layout L;
   layout_for(*dims, M, L);
@@ -310,6 +312,7 @@ static int layer_impl(const moe_layer_dims* dims, const moe_layer_weights* w, in
   na.x = nullptr; na.residual = residual; na.gain = w->norm_gain;
   na.rows = ea.rows; na.route_w = ra.tw; na.shared = has_shared ? ea.shared_out : nullptr;
   na.shared_parts = parts;
+  na.m_out = m_out;
   na.out = out; na.residual_out = residual_out; na.M = M; na.H = H; na.k = k; na.eps = dims->rms_eps;
   // the residual and the gain were written before the router's plain launch,
   // so the boundary may load them before it waits on the expert kernel
@@ -334,6 +337,30 @@ int moe_decode_layer_traced(const moe_layer_dims* dims, const moe_layer_weights*
   if (!events || !events[0] || !events[1] || !events[2] || !events[3]) return MOE_ERR_INVALID_ARG;
   return layer_impl(dims, w, M, x, residual, out, residual_out, topk_ids, topk_w, sorted_routes,
                     expert_offsets, workspace, ws_bytes, stream, events);
+}
+
+int moe_decode_layer_partial(const moe_layer_dims* dims, const moe_layer_weights* w, int M, const void* x,
+                             float* m_out, int32_t* topk_ids, float* topk_w, int32_t* sorted_routes,
+                             int32_t* expert_offsets, void* workspace, size_t ws_bytes, void* stream) {
+  if (!m_out && M > 0) return MOE_ERR_INVALID_ARG;  // (M == 0 returns before any pointer is used)
+  return layer_impl(dims, w, M, x, nullptr, nullptr, nullptr, topk_ids, topk_w, sorted_routes, expert_offsets,
+                    workspace, ws_bytes, stream, nullptr, m_out);
+}
+
+int moe_tp_boundary(const float* partials, int G, const void* residual, const void* gain, int M, int H, float eps,
+                    void* out, void* residual_out, void* stream) {
+  if (M < 0 || H <= 0 || G < 1 || !(eps >= 0.f)) return MOE_ERR_INVALID_ARG;
+  if (H % kBlock || H > 16384) return MOE_ERR_UNSUPPORTED;
+  if (!partials || !residual || !gain || !out || !residual_out) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(partials) || !aligned16(residual) || !aligned16(gain) || !aligned16(out) || !aligned16(residual_out))
+    return MOE_ERR_INVALID_ARG;
+  if (M == 0) return MOE_OK;
+  NormArgs na;
+  na.x = nullptr; na.residual = residual; na.gain = gain; na.rows = nullptr; na.route_w = nullptr;
+  na.shared = partials; na.shared_parts = G; na.m_out = nullptr;
+  na.out = out; na.residual_out = residual_out; na.M = M; na.H = H; na.k = 0; na.eps = eps;
+  na.early = 0;  // the partials may come from the kernel just before
+  return launch_rmsnorm(na, (cudaStream_t)stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 int splitk_gemm_workspace_size(int M, int N, int K, int split_k, size_t* bytes) {
@@ -381,7 +408,8 @@ int rmsnorm_residual(const void* x, const void* residual, const void* gain, int 
   if (M == 0) return MOE_OK;
   NormArgs na;
   na.x = x; na.residual = residual; na.gain = gain; na.rows = rows; na.route_w = route_w;
-  na.shared = shared; na.shared_parts = 1; na.out = out; na.residual_out = residual_out; na.M = M; na.H = H;
+  na.shared = shared; na.shared_parts = 1; na.m_out = nullptr; na.out = out; na.residual_out = residual_out;
+  na.M = M; na.H = H;
   na.k = rows ? k : 0; na.eps = eps;
   na.early = 0;  // the preceding kernel may be the one that writes them
   return launch_rmsnorm(na, (cudaStream_t)stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

@@ -160,6 +160,7 @@ struct NormArgs {
   void* out; void* residual_out;
   int M, H, k;
   int shared_parts;  // partial rows [parts][M][H] in `shared`, added in order (>= 1)
+  float* m_out;      // non-null: write m (fp32 [M, H]) there and stop (no residual, no norm)
   float eps;
   int early;  // residual and gain come from before the preceding kernels (the layer call)
 };

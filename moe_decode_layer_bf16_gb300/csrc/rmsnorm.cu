@@ -57,9 +57,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 2)
       }
     }
   };
-  if (a.early) load_inputs();
+  const bool partial = a.m_out != nullptr;  // the same in every CTA
+  if (a.early && !partial) load_inputs();
   grid_dep_wait();  // the rows come from the preceding expert kernel
-  if (!a.early) load_inputs();
+  if (!a.early && !partial) load_inputs();
 
   float ss = 0.f;
 #pragma unroll
@@ -95,6 +96,10 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 2)
         m[0] += r.x; m[1] += r.y; m[2] += r.z; m[3] += r.w;
       }
     }
+    if (partial) {  // a rank's partial sum of a tensor-parallel layer: fp32 m, nothing else
+      *reinterpret_cast<float4*>(a.m_out + rowo + j) = make_float4(m[0], m[1], m[2], m[3]);
+      continue;
+    }
     const float r0 = m[0] + bf16_lo(rv[i].x), r1 = m[1] + bf16_hi(rv[i].x);
     const float r2 = m[2] + bf16_lo(rv[i].y), r3 = m[3] + bf16_hi(rv[i].y);
     const uint32_t p01 = pack_bf16(r0, r1), p23 = pack_bf16(r2, r3);
@@ -103,6 +108,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 2)
     s_rb[j] = b0; s_rb[j + 1] = b1; s_rb[j + 2] = b2; s_rb[j + 3] = b3;
     ss += b0 * b0 + b1 * b1 + b2 * b2 + b3 * b3;
   }
+  if (partial) return;  // (uniform: no CTA of the cluster reaches its barriers)
   ss = warp_sum(ss);
   if (lane == 0) s_warp[warp] = ss;
   __syncthreads();

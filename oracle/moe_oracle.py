@@ -40,7 +40,9 @@ MLP when k = E with equal scores; the split-K GEMM against a float64 matmul;
 the MTP front's concatenation order and normalisation through projections
 that select one half (unit RMS of the selected half, the gathered row); the
 finalize's slot-to-row pairing through one-hot rows with distinct weights,
-and the routed scaling through the linearity of the routed part of m.
+and the routed scaling through the linearity of the routed part of m; the
+tensor-parallel shards through their sum, which must equal the whole layer's
+m (and their h, the matching slices of the whole layer's h).
 The full layer on real shapes is pinned only through these pieces.
 """
 
@@ -392,6 +394,58 @@ def moe_decode_layer(layer: Layer, x_bf16, residual_bf16, tokens=None):
                 sorted_routes=sorted_routes, offsets=offsets, xq=xq, xs=xs,
                 rows=rows, shared=shared, h_rows=h_rows, m=m, tokens=tokens,
                 out=out, residual_out=res_out)
+
+
+# --------------------------------------------------------------------------
+# Tensor parallelism over each expert's intermediate dimension ([decode page]
+# LayerStages: the MoE sublayer is left TP-partial; [draft page] module
+# docstring: the boundary fuses the all-reduce with the residual add and the
+# RMSNorm).  The reading: rank g of G keeps the gate rows [g I/G, (g+1) I/G),
+# the same up rows and the same w2 columns of every expert, with their block
+# scales (I/G a multiple of 128); the router is replicated.
+# --------------------------------------------------------------------------
+
+def tp_shard(layer: Layer, g: int, G: int) -> Layer:
+    """Rank g of G's share of a layer (numpy weight arrays)."""
+    def w13_rows(codes, scales, a, b):
+        inter = codes.shape[-2] // 2
+        c = np.concatenate([codes[..., a:b, :], codes[..., inter + a:inter + b, :]], axis=-2)
+        s = np.concatenate([scales[..., a // BLOCK:b // BLOCK, :],
+                            scales[..., (inter + a) // BLOCK:(inter + b) // BLOCK, :]], axis=-2)
+        return c, s
+
+    def w2_cols(codes, scales, a, b):
+        return codes[..., a:b], scales[..., a // BLOCK:b // BLOCK]
+
+    def cut(n):
+        assert n % (G * BLOCK) == 0, "shards of whole 128-blocks"
+        return g * n // G, (g + 1) * n // G
+
+    kw = {}
+    if layer.w13 is not None:
+        a, b = cut(layer.w13.shape[-2] // 2)
+        kw["w13"], kw["w13_s"] = w13_rows(layer.w13, layer.w13_s, a, b)
+        kw["w2"], kw["w2_s"] = w2_cols(layer.w2, layer.w2_s, a, b)
+    else:
+        kw.update(w13=None, w13_s=None, w2=None, w2_s=None)
+    if layer.has_shared:
+        a, b = cut(layer.sw13.shape[-2] // 2)
+        kw["sw13"], kw["sw13_s"] = w13_rows(layer.sw13, layer.sw13_s, a, b)
+        kw["sw2"], kw["sw2_s"] = w2_cols(layer.sw2, layer.sw2_s, a, b)
+    else:
+        kw.update(sw13=None, sw13_s=None, sw2=None, sw2_s=None)
+    return Layer(router_w=layer.router_w, sel_bias=layer.sel_bias, gain=layer.gain, top_k=layer.top_k,
+                 routed_scaling=layer.routed_scaling, swiglu_limit=layer.swiglu_limit, rms_eps=layer.rms_eps,
+                 e8m0=layer.e8m0, has_shared=layer.has_shared, **kw)
+
+
+def tp_boundary(partials, residual_bf16, gain_bf16, eps):
+    """The boundary over the ranks' shares of m: their sum (in rank order),
+    then the residual add and RMSNorm of rmsnorm_residual."""
+    m = np.zeros_like(np.asarray(partials[0], np.float64))
+    for p in partials:
+        m = m + np.asarray(p, np.float64)
+    return rmsnorm_residual(m, residual_bf16, gain_bf16, eps)
 
 
 # --------------------------------------------------------------------------

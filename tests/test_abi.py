@@ -208,3 +208,24 @@ def test_workspace_covers_split_dense_rows(L):
     sizes = [m.moe_decode_workspace_size(DSV3_DENSE, t) for t in range(60, 70)]
     assert sizes == sorted(sizes)
     assert sizes[4] >= 16 * 64 * 7168 * 4  # 64 tokens, up to 16 segments of fp32 rows
+
+
+def test_tp_entry_points_reject_before_launch(L):
+    fake = ctypes.c_void_p(0x10000)
+    tb = L.moe_tp_boundary
+    assert tb(fake, 0, fake, fake, 4, 512, 1e-6, fake, fake, None) == m.MOE_ERR_INVALID_ARG   # G = 0
+    assert tb(fake, 2, fake, fake, 4, 500, 1e-6, fake, fake, None) == m.MOE_ERR_UNSUPPORTED   # H % 128
+    assert tb(None, 2, fake, fake, 4, 512, 1e-6, fake, fake, None) == m.MOE_ERR_INVALID_ARG
+    assert tb(fake, 2, fake, fake, 0, 512, 1e-6, fake, fake, None) == m.MOE_OK                # M = 0
+    d = m._dims(TINY)
+    need = m.moe_decode_workspace_size(TINY, 4)
+    w = m._Weights(*[0x10000] * len(m._WEIGHT_FIELDS))
+    part = L.moe_decode_layer_partial
+    # no m_out: invalid; M = 0: a no-op whatever the pointers
+    assert part(ctypes.byref(d), ctypes.byref(w), 4, fake, None, None, None, None, None, fake, need, None) == \
+        m.MOE_ERR_INVALID_ARG
+    assert part(ctypes.byref(d), ctypes.byref(w), 0, None, None, None, None, None, None, None, 0, None) == m.MOE_OK
+    # a rank's shard needs no norm gain, but its workspace must fit
+    w.norm_gain = None
+    assert part(ctypes.byref(d), ctypes.byref(w), 4, fake, fake, None, None, None, None, fake, need - 1, None) == \
+        m.MOE_ERR_WORKSPACE_TOO_SMALL

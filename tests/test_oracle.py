@@ -379,3 +379,46 @@ def test_routed_part_scales_linearly_with_routed_scaling():
     ra, rb = a["m"] - a["shared"], b["m"] - b["shared"]
     assert np.abs(rb).max() > 0.01
     assert np.allclose(ra, 2.5 * rb, rtol=1e-12, atol=1e-12)
+
+
+# ------------------------------------------------------------ tensor parallelism
+
+@pytest.mark.parametrize("G", [2, 4])
+def test_tp_shards_sum_to_the_full_layer(G):
+    # each rank keeps I/G of every expert; the ranks' shares of m must add up
+    # to the whole layer's m, their h must be slices of the whole layer's h
+    # (no quantisation group straddles two ranks), and the boundary over the
+    # shares must give the whole layer's outputs
+    dims = TINY.with_(inter=512, shared_inter=512)
+    lw = synth.make_layer(dims, seed=9)
+    L = oracle_layer(dims, lw)
+    x, res, _ = tie_free_tokens(dims, lw, 5, seed=9)
+    full = orc.moe_decode_layer(L, to_np(x), to_np(res))
+    parts = [orc.moe_decode_layer(orc.tp_shard(L, g, G), to_np(x), to_np(res)) for g in range(G)]
+    for p in parts:
+        assert np.array_equal(p["ids"], full["ids"]) and np.array_equal(p["sorted_routes"], full["sorted_routes"])
+    msum = sum(p["m"] for p in parts)
+    assert np.allclose(msum, full["m"], rtol=1e-10, atol=1e-12)
+    I = dims.inter // G
+    for r, h in full["h_rows"].items():
+        for g, p in enumerate(parts):
+            assert np.allclose(p["h_rows"][r], h[g * I:(g + 1) * I], rtol=1e-6, atol=1e-7)
+    out, ro = orc.tp_boundary([p["m"] for p in parts], to_np(res), L.gain, L.rms_eps)
+    # the same m up to float64 summation order: equal bf16 outputs, or one bf16 step apart
+    assert np.all(np.abs(out - full["out"]) <= np.abs(full["out"]) * 2.0 ** -7)
+    assert np.all(np.abs(ro - full["residual_out"]) <= np.abs(full["residual_out"]) * 2.0 ** -7)
+
+
+def test_tp_shard_with_a_wrong_slice_is_caught():
+    # the sum pin catches a shard that takes the up rows from the wrong place
+    dims = TINY.with_(inter=512, shared_inter=512)
+    lw = synth.make_layer(dims, seed=10)
+    L = oracle_layer(dims, lw)
+    x, res, _ = tie_free_tokens(dims, lw, 3, seed=10)
+    full = orc.moe_decode_layer(L, to_np(x), to_np(res))
+    parts = [orc.tp_shard(L, g, 2) for g in range(2)]
+    bad = parts[1]
+    bad.w13 = bad.w13.copy()
+    bad.w13[:, 256:, :] = L.w13[:, 256:512, :]  # rank 1's up rows replaced by gate rows
+    ms = [orc.moe_decode_layer(p, to_np(x), to_np(res))["m"] for p in parts]
+    assert not np.allclose(ms[0] + ms[1], full["m"], rtol=1e-3, atol=1e-3)
