@@ -381,7 +381,7 @@ def timed(fn, flush_l2, reps, warm=1):
     return times
 
 
-def splitk_proj(m, flush_l2, dev, N, K, Ms=(1, 2, 4, 8, 16), reps=5, fp32=False, peak=None):
+def splitk_proj(m, flush_l2, dev, N, K, Ms=(1, 2, 4, 8, 16), reps=20, fp32=False, peak=None):
     """The split-K BF16 projection Y[M, N] = A[M, K] W[N, K]^T, L2 flushed
     before every call: us and GB/s (weights + activations in + out)."""
     res = {}
@@ -391,7 +391,7 @@ def splitk_proj(m, flush_l2, dev, N, K, Ms=(1, 2, 4, 8, 16), reps=5, fp32=False,
         w = w_m if w is None else w
         c = torch.empty((M, N), dtype=torch.float32 if fp32 else torch.bfloat16, device=dev)
         ws = torch.zeros(m.splitk_gemm_workspace_size(M, N, K), dtype=torch.uint8, device=dev)
-        us = 1e3 * statistics.median(timed(lambda: m.splitk_gemm_bf16(a, w, c, ws), flush_l2, reps))
+        us = 1e3 * statistics.fmean(timed(lambda: m.splitk_gemm_bf16(a, w, c, ws), flush_l2, reps))
         nbytes = 2 * N * K + 2 * M * K + c.element_size() * M * N
         res[str(M)] = {"us": round(us, 2), "gbps": round(nbytes / us / 1e3, 1)}
         if peak:
@@ -401,7 +401,7 @@ def splitk_proj(m, flush_l2, dev, N, K, Ms=(1, 2, 4, 8, 16), reps=5, fp32=False,
     return res
 
 
-def layer_block(m, dims, lw, Ms, flush_l2, dev, peak, reps=5, zipf=False, seed=500):
+def layer_block(m, dims, lw, Ms, flush_l2, dev, peak, reps=20, zipf=False, seed=500):
     """One layer's calls at each M (L2 flushed before every call): the plain
     call's us, tokens/s and GB/s of the layer's algorithmic bytes, and the
     expert kernel's us from a traced call (events between the kernels)."""
@@ -422,7 +422,7 @@ def layer_block(m, dims, lw, Ms, flush_l2, dev, peak, reps=5, zipf=False, seed=5
         if lay.status() != m.MOE_OK:
             raise RuntimeError("layer status")
         unique = int(torch.unique(ids).numel())
-        us, ue = 1e3 * statistics.median(plain), 1e3 * statistics.median(exp_ms)
+        us, ue = 1e3 * statistics.fmean(plain), 1e3 * statistics.fmean(exp_ms)
         lb = layer_bytes(M, unique)
         res[str(M)] = {"us_per_layer": round(us, 2), "tokens_per_s": round(M * 1e6 / us, 1),
                        "unique_experts": unique, "layer_gbps": round(lb / us / 1e3, 1),
@@ -435,7 +435,7 @@ def layer_block(m, dims, lw, Ms, flush_l2, dev, peak, reps=5, zipf=False, seed=5
     return res
 
 
-def mtp_front(m, flush_l2, dev, Ms=(1, 4, 16), reps=5):
+def mtp_front(m, flush_l2, dev, Ms=(1, 4, 16), reps=20):
     """mtp_eh_front at DeepSeek-V3 sizes (H = 7168, vocabulary 129280,
     eh_proj [7168, 14336]), L2 flushed before every call."""
     H, V = 7168, 129280
@@ -462,7 +462,7 @@ def mtp_front(m, flush_l2, dev, Ms=(1, 4, 16), reps=5):
                 times.append(e0.elapsed_time(e1))
         if m.moe_device_status(ws) != m.MOE_OK:
             raise RuntimeError("mtp_eh_front status")
-        us = 1e3 * statistics.median(times)
+        us = 1e3 * statistics.fmean(times)
         nbytes = 2 * H * 2 * H + M * (2 * H * 3 + 2 * H * 2 * 2 + 4)  # weights; e, h in, A out + in, out
         res[str(M)] = {"us": round(us, 2), "gbps": round(nbytes / us / 1e3, 1)}
     del embed, w
@@ -470,7 +470,7 @@ def mtp_front(m, flush_l2, dev, Ms=(1, 4, 16), reps=5):
     return res
 
 
-def dense_layer(m, flush_l2, dev, MS, reps=5):
+def dense_layer(m, flush_l2, dev, MS, reps=20):
     """A DeepSeek-V3 dense layer (num_experts = 0: the 18432-wide FP8 MLP in the
     shared-expert slot, no router) with its boundary, L2 flushed before every call."""
     from moe_decode_layer_bf16_gb300.dims import DSV3_DENSE as D
@@ -493,7 +493,7 @@ def dense_layer(m, flush_l2, dev, MS, reps=5):
                 times.append(e0.elapsed_time(e1))
         if lay.status() != m.MOE_OK:
             raise RuntimeError("dense layer status")
-        us = 1e3 * statistics.median(times)
+        us = 1e3 * statistics.fmean(times)
         nbytes = wbytes + 4 * M * D.hidden * 2 + D.hidden * 2
         res[str(M)] = {"us_per_layer": round(us, 2), "tokens_per_s": round(M * 1e6 / us, 1),
                        "gbps": round(nbytes / us / 1e3, 1)}
@@ -502,7 +502,7 @@ def dense_layer(m, flush_l2, dev, MS, reps=5):
     return res
 
 
-def tp_rank_partial(m, dims, lw, Ms, flush_l2, dev, peak, Gs=(2, 4, 8), reps=5):
+def tp_rank_partial(m, dims, lw, Ms, flush_l2, dev, peak, Gs=(2, 4, 8), reps=20):
     """One rank's share of the layer under G-way tensor parallelism over each
     expert's intermediate dimension (rank 0's shard through
     moe_decode_layer_partial), and the boundary over G shares.  The all-reduce
@@ -519,7 +519,7 @@ def tp_rank_partial(m, dims, lw, Ms, flush_l2, dev, peak, Gs=(2, 4, 8), reps=5):
             x, r = synth.make_tokens(M, dims.hidden, seed=700 + M, device=dev)
             mo = torch.empty((M, dims.hidden), dtype=torch.float32, device=dev)
             ids = torch.empty((M, dims.top_k), dtype=torch.int32, device=dev)
-            us = 1e3 * statistics.median(
+            us = 1e3 * statistics.fmean(
                 timed(lambda: m.moe_decode_layer_partial(sd, shard, x, mo, ws, topk_ids=ids), flush_l2, reps))
             if m.moe_device_status(ws) != m.MOE_OK:
                 raise RuntimeError("tp partial status")
@@ -527,7 +527,7 @@ def tp_rank_partial(m, dims, lw, Ms, flush_l2, dev, peak, Gs=(2, 4, 8), reps=5):
             nbytes = (unique + 1) * EXPERT_BYTES / G + ROUTER_BYTES + M * dims.hidden * (2 + 4)
             parts = torch.zeros((G, M, dims.hidden), dtype=torch.float32, device=dev)
             o, ro = torch.empty_like(x), torch.empty_like(r)
-            ub = 1e3 * statistics.median(
+            ub = 1e3 * statistics.fmean(
                 timed(lambda: m.moe_tp_boundary(parts, r, lw["gain"], o, ro, dims.rms_eps), flush_l2, reps))
             per[str(M)] = {"us_rank": round(us, 2), "rank_gbps": round(nbytes / us / 1e3, 1),
                            "rank_frac_of_measured": round(nbytes / us / 1e3 / peak, 3),
@@ -682,13 +682,16 @@ def run_ours(args, world, rank, local):
         eb = (unique[M] + 1) * EXPERT_BYTES
         exp_bytes_all += eb * args.steps
         lb = layer_bytes(M, unique[M])
-        us = 1e3 * statistics.median(layer_ms)
-        per_m[str(M)] = {"us_per_layer": round(us, 2), "tokens_per_s": round(M * 1e6 / us, 1),
+        # (CUDA event stamps here tick in steps of about 2 us: a median is a
+        # multiple of that, the mean resolves finer differences)
+        us = 1e3 * statistics.fmean(layer_ms)
+        per_m[str(M)] = {"us_per_layer": round(us, 2), "us_median": round(1e3 * statistics.median(layer_ms), 2),
+                         "tokens_per_s": round(M * 1e6 / us, 1),
                          "unique_experts": unique[M], "layer_bytes": lb,
                          "layer_gbps": round(lb / us / 1e3, 1),
-                         "us_router": round(1e3 * statistics.median(rt_ms), 2),
-                         "us_experts": round(1e3 * statistics.median(exp_ms), 2),
-                         "us_boundary": round(1e3 * statistics.median(nm_ms), 2)}
+                         "us_router": round(1e3 * statistics.fmean(rt_ms), 2),
+                         "us_experts": round(1e3 * statistics.fmean(exp_ms), 2),
+                         "us_boundary": round(1e3 * statistics.fmean(nm_ms), 2)}
     # replicas: every rank runs the same steps; the job's time is the slowest rank's
     total_ms = max_over_ranks(total_ms, world)
     value = sum(MS) * args.steps * world / (total_ms / 1e3)
@@ -733,13 +736,15 @@ def run_ours(args, world, rank, local):
     if not args.no_extras:
         def attempt(key, what, fn):
             # reported, not fatal: the headline does not depend on the extras
+            if args.extras and key not in args.extras:
+                return
             try:
                 extra[key] = {"what": what, "per_m": fn()}
             except Exception as exc:
                 extra[key] = {"what": what, "error": f"{type(exc).__name__}: {exc}"}
 
         attempt("verify_batches", "the same layer at verify / grouped batch sizes M = 64, 128, 256 (i.i.d. router "
-                "logits: nearly every expert active), L2 flushed, median of 5; us_experts from a traced call",
+                "logits: nearly every expert active), L2 flushed, mean of 20 (event stamps tick in about 2 us steps); us_experts from a traced call",
                 lambda: layer_block(m, dims, lw, (64, 128, 256), flush_l2, dev, peak))
         if dims.num_experts == DSV3.num_experts:
             def skewed():
@@ -752,29 +757,29 @@ def run_ours(args, world, rank, local):
                     torch.cuda.empty_cache()
 
             attempt("skewed_e8m0", "the DeepSeek-V3-shaped layer with power-of-two (e8m0) scales, a selection bias "
-                    "~N(0,0.5) and Zipf(1.1) expert popularity, M = 1, 16, 128, L2 flushed, median of 5",
+                    "~N(0,0.5) and Zipf(1.1) expert popularity, M = 1, 16, 128, L2 flushed, mean of 20 (event stamps tick in about 2 us steps)",
                     skewed)
         attempt("splitk_eh_proj", "splitk_gemm_bf16 (split_k = 0: stream-K), MTP eh_proj N=7168 K=14336 "
-                "(205.5 MB), L2 flushed, median of 5",
+                "(205.5 MB), L2 flushed, mean of 20 (event stamps tick in about 2 us steps)",
                 lambda: splitk_proj(m, flush_l2, dev, 7168, 14336, peak=peak))
         attempt("router_gemv", "the router GEMV alone as the split-K projection's fp32 form, "
                 "[M,7168] x [256,7168]^T -> fp32 logits (3.67 MB: launch-bound, its fraction of the HBM "
-                "roofline is not meaningful), L2 flushed, median of 5",
+                "roofline is not meaningful), L2 flushed, mean of 20 (event stamps tick in about 2 us steps)",
                 lambda: splitk_proj(m, flush_l2, dev, 256, 7168, fp32=True))
         if dims.num_experts == DSV3.num_experts:
             attempt("tp_rank_partial", "G-way tensor parallelism over each expert's intermediate dimension: one "
                     "rank's share of the layer (moe_decode_layer_partial on rank 0's shard, 1/G of every expert's "
                     "bytes) and the boundary over G shares (moe_tp_boundary); the all-reduce between GPUs is not "
-                    "measured (one GPU), L2 flushed, median of 5",
+                    "measured (one GPU), L2 flushed, mean of 20 (event stamps tick in about 2 us steps)",
                     lambda: tp_rank_partial(m, dims, lw, MS, flush_l2, dev, peak))
         attempt("graph_chain", "3 layers with distinct weights captured as one CUDA graph, each layer's outputs "
                 "feeding the next, replayed back to back without L2 flushes",
                 lambda: graph_chain(m, dims, lw, MS, 3, 10, dev))
         attempt("dense_layer", "DeepSeek-V3 dense layer (FP8 MLP 7168 x 18432, 396 MB) with its boundary, "
-                "L2 flushed, median of 5", lambda: dense_layer(m, flush_l2, dev, MS))
+                "L2 flushed, mean of 20 (event stamps tick in about 2 us steps)", lambda: dense_layer(m, flush_l2, dev, MS))
         attempt("mtp_eh_front", "mtp_eh_front, H=7168, vocab 129280, eh_proj [7168, 14336] (205.5 MB), "
-                "L2 flushed, median of 5", lambda: mtp_front(m, flush_l2, dev))
-        attempt("splitk_lm_head", "splitk_gemm_bf16, LM head N=129280 K=7168 (1.85 GB), L2 flushed, median of 5",
+                "L2 flushed, mean of 20 (event stamps tick in about 2 us steps)", lambda: mtp_front(m, flush_l2, dev))
+        attempt("splitk_lm_head", "splitk_gemm_bf16, LM head N=129280 K=7168 (1.85 GB), L2 flushed, mean of 20 (event stamps tick in about 2 us steps)",
                 lambda: splitk_proj(m, flush_l2, dev, 129280, 7168, Ms=(1, 8), peak=peak))
 
     cpu = None
@@ -785,7 +790,7 @@ def run_ours(args, world, rank, local):
             cpu["all_cores"] = oracle_all_cores(seed=0)
         except Exception as exc:
             cpu["all_cores"] = {"error": f"{type(exc).__name__}: {exc}"}
-        if not args.no_extras:
+        if not args.no_extras and (not args.extras or "oracle_per_config" in args.extras):
             try:
                 extra["oracle_per_config"] = {"what": "the oracle (one core) on one token of each workload",
                                               "per_config": oracle_per_config(seed=0)}
@@ -833,6 +838,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the other workloads (verify batches, skewed routing, split-K, router, graph chain, "
                          "dense layer, MTP front, LM head)")
+    ap.add_argument("--extras", nargs="+", default=None,
+                    help="run only these of the other workloads (by their keys in the JSON line's extra)")
     # profiling aids (smaller resident layer for multi-pass ncu captures)
     ap.add_argument("--num-experts", type=int, default=DSV3.num_experts)
     ap.add_argument("--ms", type=int, nargs="+", default=list(MS))

@@ -290,7 +290,11 @@ int rmsnorm_residual(const void *x, const void *residual, const void *gain, int 
  *               call, at byte offset 256, bf16 [M, 2H]) and the split-K sums
  * Limits: 1 <= M <= 256, H % 128 == 0, H <= 16384, vocab >= 1; 16-byte aligned
  * pointers.  Argument errors return before anything is enqueued.  Calls that
- * share a workspace must be stream-ordered. */
+ * share a workspace must be stream-ordered.
+ * Two kernels: the norm kernel, then the projection, launched with
+ * programmatic dependent launch so that it prefetches its first weight tiles
+ * into L2 while the norm kernel runs (eh_proj_w must not be written by the
+ * kernel enqueued just before the call). */
 int mtp_eh_front_workspace_size(int M, int H, size_t *bytes);
 int mtp_eh_front(const int32_t *input_ids, const void *embed, int vocab, const void *hidden,
                  const void *enorm, const void *hnorm, float eps, const void *eh_proj_w, int M, int H,

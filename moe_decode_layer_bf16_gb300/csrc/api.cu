@@ -176,6 +176,28 @@ size_t splitk_ticket_bytes(const GemvPlan& p) { return align_up((size_t)p.n_chun
 
 size_t splitk_partial_bytes(const GemvPlan& p) { return p.max_segs > 1 ? gemv_partials_bytes(p) : 0; }
 
+// splitk_gemm_bf16 with the launch form: pdl lets the kernel start while the
+// preceding kernel of the stream, which writes A (never W), still runs.
+int splitk_impl(const void* A, const void* W, void* C, int c_fp32, int M, int N, int K, int split_k, float alpha,
+                void* ws, size_t ws_bytes, void* stream, bool pdl) {
+  size_t need = 0;
+  int rc = splitk_gemm_workspace_size(M, N, K, split_k, &need);
+  if (rc != MOE_OK) return rc;
+  if (!A || !W || !C || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(A) || !aligned16(W) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  GemvPlan plan;
+  if ((rc = plan_splitk(plan, M, N, K, split_k)) != MOE_OK) return rc;
+  const size_t tickets = splitk_ticket_bytes(plan);
+  if (tickets + splitk_partial_bytes(plan) > need) return MOE_ERR_UNSUPPORTED;
+  SplitKArgs a;
+  a.A = A; a.W = W; a.C = C; a.c_fp32 = c_fp32 ? 1 : 0; a.alpha = alpha;
+  a.tickets = reinterpret_cast<unsigned*>(ws);
+  a.partials = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + tickets);
+  a.pdl = pdl;
+  return launch_splitk(plan, a, (cudaStream_t)stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -378,21 +400,7 @@ int splitk_gemm_workspace_size(int M, int N, int K, int split_k, size_t* bytes) 
 
 int splitk_gemm_bf16(const void* A, const void* W, void* C, int c_fp32, int M, int N, int K, int split_k,
                      float alpha, void* ws, size_t ws_bytes, void* stream) {
-  size_t need = 0;
-  int rc = splitk_gemm_workspace_size(M, N, K, split_k, &need);
-  if (rc != MOE_OK) return rc;
-  if (!A || !W || !C || !ws) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(A) || !aligned16(W) || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
-  if (ws_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
-  GemvPlan plan;
-  if ((rc = plan_splitk(plan, M, N, K, split_k)) != MOE_OK) return rc;
-  const size_t tickets = splitk_ticket_bytes(plan);
-  if (tickets + splitk_partial_bytes(plan) > need) return MOE_ERR_UNSUPPORTED;
-  SplitKArgs a;
-  a.A = A; a.W = W; a.C = C; a.c_fp32 = c_fp32 ? 1 : 0; a.alpha = alpha;
-  a.tickets = reinterpret_cast<unsigned*>(ws);
-  a.partials = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ws) + tickets);
-  return launch_splitk(plan, a, (cudaStream_t)stream) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return splitk_impl(A, W, C, c_fp32, M, N, K, split_k, alpha, ws, ws_bytes, stream, false);
 }
 
 int rmsnorm_residual(const void* x, const void* residual, const void* gain, int M, int H, float eps,
@@ -449,7 +457,8 @@ int mtp_eh_front(const int32_t* input_ids, const void* embed, int vocab, const v
   ea.eps = eps; ea.out = A; ea.M = M; ea.H = H;
   ea.status = reinterpret_cast<int*>(w) + kHdrStatus;
   if (launch_eh_norm(ea, (cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
-  return splitk_gemm_bf16(A, eh_proj_w, out, 0, M, H, 2 * H, 0, 1.f, gemm_ws, need - (gemm_ws - w), stream);
+  // the projection's weights stream while the norm kernel still runs
+  return splitk_impl(A, eh_proj_w, out, 0, M, H, 2 * H, 0, 1.f, gemm_ws, need - (gemm_ws - w), stream, true);
 }
 
 int moe_set_expert_path(int path) {

@@ -44,6 +44,22 @@ MOE_DEV int ld_acquire(const int* p) {
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
+// Counter updates that publish (release) what this thread, and through a
+// preceding CTA barrier its CTA, wrote before, and (acq_rel) acquire what the
+// earlier updaters published: one instruction instead of fence + atomic.
+MOE_DEV int atom_add_acq_rel(int* p, int v) {
+  int r;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(r) : "l"(p), "r"(v) : "memory");
+  return r;
+}
+MOE_DEV unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned r;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(r) : "l"(p), "r"(v) : "memory");
+  return r;
+}
+MOE_DEV void red_add_release(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 // Programmatic dependent launch: a kernel launched with programmatic stream
 // serialisation may start while its predecessor is still running; it waits
 // here before touching the predecessor's results.  A no-op otherwise.

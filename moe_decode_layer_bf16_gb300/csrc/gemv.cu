@@ -152,13 +152,11 @@ __device__ void gemv_streamk(const Gemv& d, Epi epi, OnTile on_tile) {
       }
       __syncthreads();
       if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned old = atomicAdd(d.tickets + ct, 1u);
+        const unsigned old = atom_add_acq_rel(d.tickets + ct, 1u);
         s_last = (old == (unsigned)(nseg - 1));
       }
       __syncthreads();
       if (s_last) {
-        __threadfence();
         const float* P0 = d.partials + (size_t)ct * d.max_segs * kTileOut;
         // only the valid tokens of the chunk; the segment loads of one output are
         // independent and issued 8 at a time, then added in segment order
@@ -187,8 +185,24 @@ __device__ void gemv_streamk(const Gemv& d, Epi epi, OnTile on_tile) {
   }
 }
 
+constexpr int kPdlCells = 4;  // cells a CTA prefetches into L2 before it waits (programmatic launch)
+
 template <int TT>
-__global__ void __launch_bounds__(kThreads) splitk_kernel(Gemv d, void* C, int c_fp32, float alpha) {
+__global__ void __launch_bounds__(kThreads) splitk_kernel(Gemv d, void* C, int c_fp32, float alpha, int pdl) {
+  if (pdl) {
+    // Launched while the kernel that writes A still runs: the weights of this
+    // CTA's first cells go into L2 (a thread a 128-byte line), then the wait.
+    const long long x0 = (long long)blockIdx.x * d.total / d.G;
+    const long long x1 = min(x0 + kPdlCells, (long long)(blockIdx.x + 1) * d.total / d.G);
+    for (long long x = x0; x < x1; ++x) {
+      const int kb = (int)(x % d.nkb), tile = (int)((x / d.nkb) % d.n_tiles);
+      const int row = tile * 64 + (threadIdx.x >> 1);
+      if (row < d.N)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(d.W + (size_t)row * d.K * 2 + (size_t)kb * 256 +
+                                                      (threadIdx.x & 1) * 128));
+    }
+    grid_dep_wait();
+  }
   auto epi = [&](int n, int r, float v) {
     v *= alpha;
     if (c_fp32)
@@ -451,8 +465,7 @@ __global__ void __launch_bounds__(kThreads) router_kernel(Gemv d, RouterDev r) {
   const int F = min(min(kMaxFinish, (d.M + 3) / 4), (int)gridDim.x);
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    const int t = atomicAdd(r.hdr + kHdrRouterTicket, 1);
+    const int t = atom_add_acq_rel(r.hdr + kHdrRouterTicket, 1);
     s_finish = t >= (int)gridDim.x - F ? t - ((int)gridDim.x - F) : -1;
   }
   __syncthreads();
@@ -473,8 +486,7 @@ __global__ void __launch_bounds__(kThreads) router_kernel(Gemv d, RouterDev r) {
   if (F > 1) {
     // the last finisher to be done orders the routes, from every finisher's ids
     if (threadIdx.x == 0) {
-      __threadfence();
-      s_finish = atomicAdd(r.hdr + kHdrRouterFin, 1) == F - 1;
+      s_finish = atom_add_acq_rel(r.hdr + kHdrRouterFin, 1) == F - 1;
     }
     __syncthreads();
     if (!s_finish) return;
@@ -547,11 +559,13 @@ int gemv_blocks_per_sm(int chunk_tokens, bool router) {
 
 cudaError_t launch_splitk(const GemvPlan& p, const SplitKArgs& a, cudaStream_t s) {
   Gemv d = make_gemv(p, a.A, a.W, a.partials, a.tickets);
-  switch (p.chunk_tokens) {
-    case 8: splitk_kernel<1><<<p.G, kThreads, 0, s>>>(d, a.C, a.c_fp32, a.alpha); break;
-    case 16: splitk_kernel<2><<<p.G, kThreads, 0, s>>>(d, a.C, a.c_fp32, a.alpha); break;
-    default: splitk_kernel<4><<<p.G, kThreads, 0, s>>>(d, a.C, a.c_fp32, a.alpha); break;
+  const int pdl = a.pdl ? 1 : 0;
+  auto kernel = p.chunk_tokens == 8 ? splitk_kernel<1> : p.chunk_tokens == 16 ? splitk_kernel<2> : splitk_kernel<4>;
+  if (a.pdl) {
+    PdlLaunch L(dim3(p.G), dim3(kThreads), 0, s);
+    return cudaLaunchKernelEx(&L.cfg, kernel, d, a.C, a.c_fp32, a.alpha, pdl);
   }
+  kernel<<<p.G, kThreads, 0, s>>>(d, a.C, a.c_fp32, a.alpha, pdl);
   return cudaGetLastError();
 }
 

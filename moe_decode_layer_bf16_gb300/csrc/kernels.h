@@ -69,6 +69,10 @@ struct SplitKArgs {
   float alpha;
   float* partials;
   unsigned* tickets;
+  // programmatic dependent launch: the kernel starts while the preceding one
+  // (which writes A, never W) ends, prefetches its first weights into L2 and
+  // waits for that kernel before it reads A
+  bool pdl = false;
 };
 cudaError_t launch_splitk(const GemvPlan& p, const SplitKArgs& a, cudaStream_t s);
 

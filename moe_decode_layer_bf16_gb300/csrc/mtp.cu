@@ -21,6 +21,7 @@ constexpr int kThreads = 512;
 
 __global__ void __launch_bounds__(kThreads) eh_norm_kernel(EhNormArgs a) {
   __shared__ float s_red[2][kThreads / 32];
+  grid_dep_launch();  // the projection may start streaming its weights now
   const int t = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int id = a.ids[t];

@@ -260,6 +260,26 @@ def test_splitk_router_form_fp32(M):
     assert orc.max_abs_rel(to_np(c), ref) <= 1e-4
 
 
+# edge shapes: a last 64-row tile of 16 rows, a single k-block (K = 128),
+# token chunks of 32 with a ragged last chunk (M = 17, 33, 255), a single
+# 16-row tile (N = 16), fewer cells than CTAs; bf16 and fp32 outputs
+@pytest.mark.parametrize("M,N,K", [(1, 1040, 128), (17, 2064, 384), (33, 512, 1024), (255, 1024, 2048),
+                                   (5, 16, 7168), (3, 7168, 256)])
+def test_splitk_edge_shapes(M, N, K):
+    a, w = synth.make_projection(M, N, K, seed=90 + M, device=DEV)
+    c = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device=DEV)
+    ws = torch.zeros(m.splitk_gemm_workspace_size(M, N, K), dtype=torch.uint8, device=DEV)
+    m.splitk_gemm_bf16(a, w, c, ws)
+    torch.cuda.synchronize()
+    ref = orc.projection(to_np(a), to_np(w))
+    assert orc.max_abs_rel(to_np(c), ref) <= 1e-2
+    c32 = torch.full((M, N), float("nan"), dtype=torch.float32, device=DEV)
+    m.splitk_gemm_bf16(a, w, c32, ws)
+    torch.cuda.synchronize()
+    ref32 = orc.projection(to_np(a), to_np(w), out_fp32=True)
+    assert orc.max_abs_rel(to_np(c32), ref32) <= 1e-4
+
+
 @pytest.mark.parametrize("M", [1, 8])
 def test_splitk_lm_head_vocab_width_sampled(M):
     # the LM-head projection at the DeepSeek-V3 vocabulary width (1.85 GB of
