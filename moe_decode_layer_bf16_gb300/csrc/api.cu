@@ -34,6 +34,24 @@ size_t gemv_partials_bound(int M, int N, int K) {
   return gemv_partials_bytes(p);
 }
 
+// The same bound for an automatic split-K plan, with or without the dynamic
+// tail: a static split over all tiles, or over all but the tail's tiles
+// (shorter runs) with the tail tiles' units.
+size_t splitk_partials_bound(int M, int N, int K) {
+  GemvPlan p;
+  p.chunk_tokens = gemv_chunk_tokens(M);
+  p.n_chunks = (M + p.chunk_tokens - 1) / p.chunk_tokens;
+  p.n_tiles = (N + 63) / 64;
+  p.nkb = K / kBlock;
+  const long long n_ct = (long long)p.n_chunks * p.n_tiles;
+  p.dyn_tiles = (int)splitk_dyn_tiles(n_ct);
+  p.dyn_nu = p.dyn_tiles > 0 ? (p.nkb + std::min(kDynUnit, p.nkb) - 1) / std::min(kDynUnit, p.nkb) : 0;
+  const long long total = (n_ct - p.dyn_tiles) * p.nkb;
+  const long long minrun = std::max<long long>(1, total / kGemvMaxCtas);
+  p.max_segs = (int)std::min<long long>(p.nkb, (p.nkb + minrun - 1) / minrun + 1);
+  return std::max(gemv_partials_bytes(p), gemv_partials_bound(M, N, K));
+}
+
 struct Layout {
   size_t hdr, tickets, gcount, ready, partials, logits, xq, xs, ids, tw, sorted, off, act;
   size_t h, hq, hs, rows, shared, xg, gu_part, total;
@@ -168,13 +186,22 @@ int plan_splitk(GemvPlan& plan, int M, int N, int K, int split_k) {
     if ((rc = current_device_sms(&sms)) != MOE_OK) return rc;
     G = gemv_grid(n_ct * (K / kBlock), sms, gemv_blocks_per_sm(gemv_chunk_tokens(M), false));
   }
-  plan_gemv(plan, M, N, K, (int)G);
+  // The dynamic tail pays where every CTA streams a long static share (each
+  // unit starts its loads cold: measured, LM head at 1.85 GB 299 -> 276 us,
+  // eh_proj at 205 MB 40.9 -> 41.4 us); an explicit split keeps every segment
+  // where it was asked for.
+  const bool tail = split_k == 0 && n_ct * (K / kBlock) >= kDynMinRun * G;
+  plan_gemv(plan, M, N, K, (int)G, tail ? (int)splitk_dyn_tiles(n_ct) : 0);
   return MOE_OK;
 }
 
-size_t splitk_ticket_bytes(const GemvPlan& p) { return align_up((size_t)p.n_chunks * p.n_tiles * sizeof(unsigned)); }
+size_t splitk_ticket_bytes(const GemvPlan& p) {
+  return align_up(((size_t)p.n_chunks * p.n_tiles + 2) * sizeof(unsigned));
+}
 
-size_t splitk_partial_bytes(const GemvPlan& p) { return p.max_segs > 1 ? gemv_partials_bytes(p) : 0; }
+size_t splitk_partial_bytes(const GemvPlan& p) {
+  return p.max_segs > 1 || p.dyn_nu > 1 ? gemv_partials_bytes(p) : 0;
+}
 
 // splitk_gemm_bf16 with the launch form: pdl lets the kernel start while the
 // preceding kernel of the stream, which writes A (never W), still runs.
@@ -391,10 +418,10 @@ int splitk_gemm_workspace_size(int M, int N, int K, int split_k, size_t* bytes) 
   if (rc != MOE_OK) return rc;
   const long long n_ct = tiles_of(M, N);
   // the automatic split depends on the device's SM count: its bound covers any grid
-  const size_t partials = split_k == 0 ? gemv_partials_bound(M, N, K)
+  const size_t partials = split_k == 0 ? splitk_partials_bound(M, N, K)
                           : split_k == 1 ? 0
                                          : (size_t)n_ct * split_k * gemv_chunk_tokens(M) * 64 * sizeof(float);
-  *bytes = align_up((size_t)n_ct * sizeof(unsigned)) + partials;
+  *bytes = align_up(((size_t)n_ct + 2) * sizeof(unsigned)) + partials;
   return MOE_OK;
 }
 

@@ -35,9 +35,10 @@ struct Gemv {
   const uint8_t* A;  // bf16 [M, K] as bytes
   const uint8_t* W;  // bf16 [N, K]
   int M, N, K, nkb, n_tiles, n_chunks, G, max_segs;
-  long long total;
+  long long total;  // statically split cells
   float* partials;
-  unsigned* tickets;
+  unsigned* tickets;  // one per (chunk, tile), then the tail's unit and exit counters
+  int dyn_tiles, dyn_unit, dyn_nu;
 };
 
 // acc[tt] holds rows (g, g+8) x tokens (2q, 2q+1) of token tile tt for this
@@ -106,15 +107,86 @@ __device__ __forceinline__ void gemv_segment(const Gemv& d, int chunk, int tile,
   }
 }
 
-// Runs this CTA's cells.  epi(token, row, value) receives every finished
-// output; on_tile() is called (by all threads, after the epilogue of a tile)
-// in the CTA that completed a (chunk, tile).
-template <int TT, class Epi, class OnTile>
-__device__ void gemv_streamk(const Gemv& d, Epi epi, OnTile on_tile) {
+// Hands over the sums of segment seg (of nseg) of (chunk, tile) ct that this
+// CTA computed: written out directly when the tile has one segment, else
+// stored as partial sums; the CTA that stores a tile's last segment adds them
+// all in segment order (deterministic) and writes the tile.  Returns whether
+// this CTA completed the tile.  Called by all threads.
+// Partial-sum slot of segment seg of (chunk, tile) ct: max_segs slots a
+// statically split tile, then dyn_nu a tile of the dynamic tail.
+__device__ __forceinline__ size_t part_slot(const Gemv& d, long long ct, int seg) {
+  const long long ns = (long long)d.n_chunks * d.n_tiles - d.dyn_tiles;
+  return (size_t)(ct < ns ? ct * d.max_segs : ns * d.max_segs + (ct - ns) * d.dyn_nu) + seg;
+}
+
+template <int TT, class Epi>
+__device__ bool finish_segment(const Gemv& d, long long ct, int seg, int nseg, const float (&acc)[TT][4], Epi epi) {
   __shared__ int s_last;
-  const int c = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
   constexpr int kTileOut = 8 * TT * 64;
+  const int chunk = (int)(ct / d.n_tiles), tile = (int)(ct % d.n_tiles);
+  const int rl0 = warp * 16 + g, rl1 = rl0 + 8;
+  if (nseg == 1) {
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+      const int n0 = chunk * 8 * TT + t * 8 + 2 * q;
+      const int r0 = tile * 64 + rl0, r1 = tile * 64 + rl1;
+      if (r0 < d.N) {
+        if (n0 < d.M) { epi(n0, r0, acc[t][0]); epi(n0, r1, acc[t][2]); }
+        if (n0 + 1 < d.M) { epi(n0 + 1, r0, acc[t][1]); epi(n0 + 1, r1, acc[t][3]); }
+      }
+    }
+    __syncthreads();
+    return true;
+  }
+  float* P = d.partials + part_slot(d, ct, seg) * kTileOut;
+#pragma unroll
+  for (int t = 0; t < TT; ++t) {
+    const int tl0 = t * 8 + 2 * q;
+    P[tl0 * 64 + rl0] = acc[t][0];
+    P[(tl0 + 1) * 64 + rl0] = acc[t][1];
+    P[tl0 * 64 + rl1] = acc[t][2];
+    P[(tl0 + 1) * 64 + rl1] = acc[t][3];
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // publishes this CTA's partial sums; the last segment's count also
+    // acquires every other segment's (the barrier below passes it on)
+    const unsigned old = atom_add_acq_rel(d.tickets + ct, 1u);
+    s_last = (old == (unsigned)(nseg - 1));
+  }
+  __syncthreads();
+  if (!s_last) return false;
+  const float* P0 = d.partials + part_slot(d, ct, 0) * kTileOut;
+  // only the valid tokens of the chunk; the segment loads of one output are
+  // independent and issued 16 at a time, then added in segment order
+  const int ntok = min(8 * TT, d.M - chunk * 8 * TT);
+  for (int idx = threadIdx.x; idx < ntok * 64; idx += kThreads) {
+    const int tl = idx >> 6, rl = idx & 63;
+    const int n = chunk * 8 * TT + tl, r = tile * 64 + rl;
+    if (r < d.N) {
+      float v = 0.f;
+      for (int s = 0; s < nseg; s += 16) {
+        float t[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) t[j] = s + j < nseg ? __ldcg(P0 + (size_t)(s + j) * kTileOut + idx) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v += t[j];
+      }
+      epi(n, r, v);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) d.tickets[ct] = 0u;
+  return true;
+}
+
+// Runs this CTA's statically assigned cells.  epi(token, row, value)
+// receives every finished output; on_tile() is called (by all threads, after
+// the epilogue of a tile) in the CTA that completed a (chunk, tile).
+template <int TT, class Epi, class OnTile>
+__device__ void gemv_streamk(const Gemv& d, Epi epi, OnTile on_tile) {
+  const int c = blockIdx.x;
   long long cur = (long long)c * d.total / d.G;
   const long long end = (long long)(c + 1) * d.total / d.G;
   while (cur < end) {
@@ -124,71 +196,48 @@ __device__ void gemv_streamk(const Gemv& d, Epi epi, OnTile on_tile) {
     const int chunk = (int)(ct / d.n_tiles), tile = (int)(ct % d.n_tiles);
     const int first = cta_of_cell(ct * d.nkb, d.total, d.G);
     const int nseg = cta_of_cell(ct * d.nkb + d.nkb - 1, d.total, d.G) - first + 1;
-    const int seg = c - first;
     float acc[TT][4];
     gemv_segment<TT>(d, chunk, tile, kb0, kb1, acc);
-    const int rl0 = warp * 16 + g, rl1 = rl0 + 8;
-    if (nseg == 1) {
-#pragma unroll
-      for (int t = 0; t < TT; ++t) {
-        const int n0 = chunk * 8 * TT + t * 8 + 2 * q;
-        const int r0 = tile * 64 + rl0, r1 = tile * 64 + rl1;
-        if (r0 < d.N) {
-          if (n0 < d.M) { epi(n0, r0, acc[t][0]); epi(n0, r1, acc[t][2]); }
-          if (n0 + 1 < d.M) { epi(n0 + 1, r0, acc[t][1]); epi(n0 + 1, r1, acc[t][3]); }
-        }
-      }
-      __syncthreads();
-      on_tile();
-    } else {
-      float* P = d.partials + ((size_t)ct * d.max_segs + seg) * kTileOut;
-#pragma unroll
-      for (int t = 0; t < TT; ++t) {
-        const int tl0 = t * 8 + 2 * q;
-        P[tl0 * 64 + rl0] = acc[t][0];
-        P[(tl0 + 1) * 64 + rl0] = acc[t][1];
-        P[tl0 * 64 + rl1] = acc[t][2];
-        P[(tl0 + 1) * 64 + rl1] = acc[t][3];
-      }
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        const unsigned old = atom_add_acq_rel(d.tickets + ct, 1u);
-        s_last = (old == (unsigned)(nseg - 1));
-      }
-      __syncthreads();
-      if (s_last) {
-        const float* P0 = d.partials + (size_t)ct * d.max_segs * kTileOut;
-        // only the valid tokens of the chunk; the segment loads of one output are
-        // independent and issued 8 at a time, then added in segment order
-        const int ntok = min(8 * TT, d.M - chunk * 8 * TT);
-        for (int idx = threadIdx.x; idx < ntok * 64; idx += kThreads) {
-          const int tl = idx >> 6, rl = idx & 63;
-          const int n = chunk * 8 * TT + tl, r = tile * 64 + rl;
-          if (r < d.N) {
-            float v = 0.f;
-            for (int s = 0; s < nseg; s += 16) {
-              float t[16];
-#pragma unroll
-              for (int j = 0; j < 16; ++j) t[j] = s + j < nseg ? __ldcg(P0 + (size_t)(s + j) * kTileOut + idx) : 0.f;
-#pragma unroll
-              for (int j = 0; j < 16; ++j) v += t[j];
-            }
-            epi(n, r, v);
-          }
-        }
-        __syncthreads();
-        if (threadIdx.x == 0) d.tickets[ct] = 0u;
-        on_tile();
-      }
-    }
+    if (finish_segment<TT>(d, ct, c - first, nseg, acc, epi)) on_tile();
     cur += kb1 - kb0;
+  }
+}
+
+// The dynamic tail: units of dyn_unit k-blocks of the last dyn_tiles (chunk,
+// tile)s, taken one at a time from the unit counter; the last CTA to leave
+// resets both tail counters for the next call.
+template <int TT, class Epi>
+__device__ void gemv_tail(const Gemv& d, Epi epi) {
+  __shared__ int s_unit;
+  const long long n_ct = (long long)d.n_chunks * d.n_tiles;
+  const int units = d.dyn_tiles * d.dyn_nu;
+  unsigned* next = d.tickets + n_ct;
+  for (;;) {
+    __syncthreads();  // (s_unit is rewritten below)
+    if (threadIdx.x == 0) s_unit = (int)atomicAdd(next, 1u);
+    __syncthreads();
+    const int u = s_unit;
+    if (u >= units) break;
+    const long long ct = n_ct - d.dyn_tiles + u / d.dyn_nu;
+    const int seg = u % d.dyn_nu;
+    const int kb0 = seg * d.dyn_unit, kb1 = min(d.nkb, kb0 + d.dyn_unit);
+    float acc[TT][4];
+    gemv_segment<TT>(d, (int)(ct / d.n_tiles), (int)(ct % d.n_tiles), kb0, kb1, acc);
+    finish_segment<TT>(d, ct, seg, d.dyn_nu, acc, epi);
+  }
+  // every CTA's last take came before its count here: the last one resets
+  if (threadIdx.x == 0 && atom_add_acq_rel(d.tickets + n_ct + 1, 1u) == (unsigned)gridDim.x - 1) {
+    d.tickets[n_ct] = 0u;
+    d.tickets[n_ct + 1] = 0u;
   }
 }
 
 constexpr int kPdlCells = 4;  // cells a CTA prefetches into L2 before it waits (programmatic launch)
 
+// (register budgets: 8-token tiles 128, 16-token 170, 32-token 256 a thread,
+// so that 4, 3 and 2 CTAs an SM keep their loads in flight)
 template <int TT>
-__global__ void __launch_bounds__(kThreads) splitk_kernel(Gemv d, void* C, int c_fp32, float alpha, int pdl) {
+__global__ void __launch_bounds__(kThreads, TT == 1 ? 4 : TT == 2 ? 3 : 2) splitk_kernel(Gemv d, void* C, int c_fp32, float alpha, int pdl) {
   if (pdl) {
     // Launched while the kernel that writes A still runs: the weights of this
     // CTA's first cells go into L2 (a thread a 128-byte line), then the wait.
@@ -211,6 +260,7 @@ __global__ void __launch_bounds__(kThreads) splitk_kernel(Gemv d, void* C, int c
       reinterpret_cast<__nv_bfloat16*>(C)[(size_t)n * d.N + r] = __float2bfloat16_rn(v);
   };
   gemv_streamk<TT>(d, epi, [] {});
+  if (d.dyn_tiles > 0) gemv_tail<TT>(d, epi);
 }
 
 // ------------------------------------------------------------------ router
@@ -393,7 +443,7 @@ __device__ void route_order(const RouterDev& r, int M, int* s_ids, bool ids_in_s
 }
 
 template <int TT>
-__global__ void __launch_bounds__(kThreads) router_kernel(Gemv d, RouterDev r) {
+__global__ void __launch_bounds__(kThreads, TT == 1 ? 4 : TT == 2 ? 3 : 2) router_kernel(Gemv d, RouterDev r) {
   __shared__ int s_finish;
   __shared__ int s_ids[kMaxMk];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -503,6 +553,7 @@ Gemv make_gemv(const GemvPlan& p, const void* A, const void* W, float* partials,
   d.G = p.G; d.max_segs = p.max_segs; d.total = p.total;
   d.partials = partials;
   d.tickets = tickets;
+  d.dyn_tiles = p.dyn_tiles; d.dyn_unit = p.dyn_unit; d.dyn_nu = p.dyn_nu;
   return d;
 }
 
@@ -512,16 +563,20 @@ static int cta_of_cell_host(long long x, long long total, int G) {
   return (int)(((x + 1) * (long long)G + total - 1) / total) - 1;
 }
 
-void plan_gemv(GemvPlan& p, int M, int N, int K, int G) {
+void plan_gemv(GemvPlan& p, int M, int N, int K, int G, int dyn_tiles) {
   p.M = M; p.N = N; p.K = K;
   p.chunk_tokens = gemv_chunk_tokens(M);
   p.n_chunks = (M + p.chunk_tokens - 1) / p.chunk_tokens;
   p.n_tiles = (N + 63) / 64;
   p.nkb = K / kBlock;
-  p.total = (long long)p.n_chunks * p.n_tiles * p.nkb;
+  const long long n_ct = (long long)p.n_chunks * p.n_tiles;
+  p.dyn_tiles = dyn_tiles;
+  p.dyn_unit = dyn_tiles > 0 ? std::min(kDynUnit, p.nkb) : 0;
+  p.dyn_nu = dyn_tiles > 0 ? (p.nkb + p.dyn_unit - 1) / p.dyn_unit : 0;
+  p.total = (n_ct - dyn_tiles) * p.nkb;
   p.G = (int)std::min<long long>(G, p.total);
   p.max_segs = 1;
-  for (long long ct = 0; ct < (long long)p.n_chunks * p.n_tiles; ++ct) {
+  for (long long ct = 0; ct < n_ct - dyn_tiles; ++ct) {
     const int a = cta_of_cell_host(ct * p.nkb, p.total, p.G);
     const int b = cta_of_cell_host(ct * p.nkb + p.nkb - 1, p.total, p.G);
     p.max_segs = std::max(p.max_segs, b - a + 1);
@@ -529,7 +584,9 @@ void plan_gemv(GemvPlan& p, int M, int N, int K, int G) {
 }
 
 size_t gemv_partials_bytes(const GemvPlan& p) {
-  return (size_t)p.n_chunks * p.n_tiles * p.max_segs * p.chunk_tokens * 64 * sizeof(float);
+  const size_t n_ct = (size_t)p.n_chunks * p.n_tiles;
+  const size_t slots = (n_ct - p.dyn_tiles) * p.max_segs + (size_t)p.dyn_tiles * p.dyn_nu;
+  return slots * p.chunk_tokens * 64 * sizeof(float);
 }
 
 int gemv_blocks_per_sm(int chunk_tokens, bool router) {

@@ -32,15 +32,25 @@ constexpr int kMaxTopK = 16;
 // Stream-K split of a skinny GEMM Y[M, N] = A[M, K] . W[N, K]^T over G CTAs.
 // Work cells are (token chunk, 64-row tile, 128-column k-block), k fastest;
 // CTA c owns cells [c*T/G, (c+1)*T/G).
+// With dyn_tiles > 0 the last dyn_tiles (chunk, tile)s are left out of the
+// static split: they are cut into units of dyn_unit k-blocks (dyn_nu a tile,
+// fixed boundaries) that the CTAs take from a counter once their static share
+// is done, so that the CTAs that stream faster take the tail.
 struct GemvPlan {
   int M, N, K;
   int chunk_tokens;  // 8, 16 or 32
   int n_chunks, n_tiles, nkb;
-  long long total;   // cells
+  long long total;   // statically split cells
   int G;             // CTAs
-  int max_segs;      // most segments that cover one (chunk, tile)
+  int max_segs;      // most static runs that cover one (chunk, tile)
+  int dyn_tiles = 0, dyn_unit = 0, dyn_nu = 0;
 };
-void plan_gemv(GemvPlan& p, int M, int N, int K, int G);
+void plan_gemv(GemvPlan& p, int M, int N, int K, int G, int dyn_tiles = 0);
+// (chunk, tile)s of the dynamic tail of an automatic split-K plan over n_ct
+// of them, and its unit length in k-blocks
+inline long long splitk_dyn_tiles(long long n_ct) { return n_ct >= 32 ? n_ct / 8 : 0; }
+constexpr int kDynUnit = 4;
+constexpr int kDynMinRun = 64;  // static cells a CTA streams at least for the tail to be used
 // resident CTAs per SM of the split-K (router == false) or router kernel on
 // the current device (cached per device)
 int gemv_blocks_per_sm(int chunk_tokens, bool router);
@@ -56,8 +66,9 @@ int current_device_sms(int* sms);
 // S K-segments, one CTA each.  Returns MOE_OK, MOE_ERR_INVALID_ARG or
 // MOE_ERR_UNSUPPORTED (shape or split out of range) or MOE_ERR_CUDA.
 int plan_splitk(GemvPlan& p, int M, int N, int K, int split_k);
-// Bytes of the plan's tile counters (one per (chunk, tile), rounded up to
-// 256) and of its partial sums (0 when no tile is split).
+// Bytes of the plan's counters (one per (chunk, tile), then the dynamic
+// tail's unit counter and exit counter; rounded up to 256) and of its partial
+// sums (0 when no tile is split).
 size_t splitk_ticket_bytes(const GemvPlan& p);
 size_t splitk_partial_bytes(const GemvPlan& p);
 

@@ -135,9 +135,10 @@ def test_splitk_rejects_before_launch(L):
         need = m.splitk_gemm_workspace_size(4, 7168, 14336, split)
         assert call(fake, 4, 7168, 14336, split, need - 1) == m.MOE_ERR_WORKSPACE_TOO_SMALL
     # an explicit split needs exactly its partial sums: tiles x S x 8 tokens x 64 rows (fp32),
-    # none when no tile is split, plus one counter per tile (rounded up to 256 bytes)
+    # none when no tile is split, plus one counter per tile and the two counters of the
+    # automatic split's dynamic tail (rounded up to 256 bytes)
     tiles = 7168 // 64
-    counters = (tiles * 4 + 255) // 256 * 256
+    counters = ((tiles + 2) * 4 + 255) // 256 * 256
     assert m.splitk_gemm_workspace_size(4, 7168, 14336, 1) == counters
     assert m.splitk_gemm_workspace_size(4, 7168, 14336, 7) == counters + tiles * 7 * 8 * 64 * 4
     nz = L.splitk_gemm_bf16_noalloc
