@@ -101,10 +101,11 @@ def load_peaks():
 
 class Clocks:
     """The SM clock and the clock-event (throttle) reasons of the GPU, sampled
-    every 10 ms from a thread while the timed region runs (NVML through ctypes:
-    a timed region of a few tens of milliseconds still gets samples), or every
-    200 ms by nvidia-smi where NVML cannot be loaded.  Reads only."""
+    every 2 ms from a thread while the timed region runs (NVML through ctypes:
+    a timed region of a few tens of milliseconds still gets tens of samples),
+    or every 200 ms by nvidia-smi where NVML cannot be loaded.  Reads only."""
 
+    PERIOD_S = 0.002
     # NVML clock-event reason bits
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
@@ -160,7 +161,7 @@ class Clocks:
                 if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0 and \
                         reasons_fn(h, ctypes.byref(rs)) == 0:
                     self.samples.append((float(clk.value), int(rs.value)))
-                time.sleep(0.01)
+                time.sleep(self.PERIOD_S)
 
         self.thread = threading.Thread(target=run, daemon=True)
         self.thread.start()
@@ -173,7 +174,8 @@ class Clocks:
                 return None
             reasons = sorted({n for _, r in self.samples for b, n in self.REASONS.items() if r & b})
             return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": self.max_mhz,
-                    "reasons": reasons, "samples": len(self.samples), "source": "nvml, 10 ms"}
+                    "reasons": reasons, "samples": len(self.samples),
+                    "source": f"nvml, {self.PERIOD_S * 1e3:g} ms"}
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -831,7 +833,7 @@ def run_ours(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
