@@ -44,7 +44,7 @@ struct Gemv {
 // acc[tt] holds rows (g, g+8) x tokens (2q, 2q+1) of token tile tt for this
 // warp's 16 rows, summed over k-blocks [kb0, kb1).
 template <int TT>
-__device__ __forceinline__ void gemv_segment(const Gemv& d, int chunk, int tile, int kb0, int kb1,
+__device__ __forceinline__ void gemv_segment_regs(const Gemv& d, int chunk, int tile, int kb0, int kb1,
                                              float (&acc)[TT][4]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
 #pragma unroll
@@ -112,6 +112,95 @@ __device__ __forceinline__ void gemv_segment(const Gemv& d, int chunk, int tile,
 // stored as partial sums; the CTA that stores a tile's last segment adds them
 // all in segment order (deterministic) and writes the tile.  Returns whether
 // this CTA completed the tile.  Called by all threads.
+constexpr int kXPitch = 256 + 16;  // bytes a token row of a staged k-block (padded: no bank conflicts)
+
+MOE_DEV void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+MOE_DEV void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+MOE_DEV void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// The same sums with the chunk's token rows staged in shared memory: the CTA
+// copies each k-block's 8 TT rows once (cp.async, double-buffered, one
+// barrier a k-block) and every warp reads its fragments from there, so that
+// only the weights of two k-blocks stay in registers (at 16 and 32 tokens the
+// register form holds the activations of two k-blocks too, which limits the
+// CTAs an SM and hence the weight bytes in flight).  Called by all threads of
+// the CTA.
+template <int TT>
+__device__ __forceinline__ void gemv_segment_smem(const Gemv& d, int chunk, int tile, int kb0, int kb1,
+                                                  float (&acc)[TT][4]) {
+  __shared__ __align__(16) uint8_t s_x[2][8 * TT][kXPitch];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
+#pragma unroll
+  for (int t = 0; t < TT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+  const int row0 = tile * 64 + warp * 16;
+  const bool rows = row0 < d.N;  // (a warp past N still stages and meets the barriers)
+  const size_t rowb = (size_t)d.K * 2;
+  const uint8_t* w0 = d.W + (size_t)(rows ? row0 + g : 0) * rowb + q * 16;
+  const uint8_t* w1 = w0 + 8 * rowb;
+  auto stage_x = [&](int kb, int buf) {
+#pragma unroll
+    for (int j = 0; j < TT; ++j) {
+      const int idx = threadIdx.x + j * kThreads;  // 16-byte piece idx of the 8 TT x 256-byte block
+      const int r = idx >> 4, c = idx & 15, n = chunk * 8 * TT + r;
+      uint8_t* dst = &s_x[buf][r][c * 16];
+      if (n < d.M) cp_async16(dst, d.A + (size_t)n * rowb + (size_t)kb * 256 + c * 16);
+      else *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    cp_async_commit();
+  };
+  uint4 c0[4], c1[4];
+  if (rows) {
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      c0[s] = ld_stream(w0 + (size_t)kb0 * 256 + s * 64);
+      c1[s] = ld_stream(w1 + (size_t)kb0 * 256 + s * 64);
+    }
+  }
+  stage_x(kb0, 0);
+#pragma unroll 1
+  for (int kb = kb0; kb < kb1; ++kb) {
+    const int buf = (kb - kb0) & 1;
+    const bool more = kb + 1 < kb1;
+    uint4 n0[4], n1[4];
+    if (more && rows) {
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        n0[s] = ld_stream(w0 + (size_t)(kb + 1) * 256 + s * 64);
+        n1[s] = ld_stream(w1 + (size_t)(kb + 1) * 256 + s * 64);
+      }
+    }
+    cp_async_wait_all();
+    // every thread's copies of this k-block have landed, and every warp is
+    // done with the other buffer (read in the previous k-block)
+    __syncthreads();
+    if (more) stage_x(kb + 1, buf ^ 1);
+    if (rows) {
+#pragma unroll
+      for (int t = 0; t < TT; ++t)
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          const uint4 b = *reinterpret_cast<const uint4*>(&s_x[buf][t * 8 + g][s * 64 + q * 16]);
+          mma_span_bf16(acc[t], c0[s], c1[s], b);
+        }
+      if (more) {
+#pragma unroll
+        for (int s = 0; s < 4; ++s) { c0[s] = n0[s]; c1[s] = n1[s]; }
+      }
+    }
+  }
+  __syncthreads();  // (the buffers are rewritten by the next segment)
+}
+
+template <int TT>
+__device__ __forceinline__ void gemv_segment(const Gemv& d, int chunk, int tile, int kb0, int kb1,
+                                             float (&acc)[TT][4]) {
+  if constexpr (TT == 1) gemv_segment_regs<TT>(d, chunk, tile, kb0, kb1, acc);
+  else gemv_segment_smem<TT>(d, chunk, tile, kb0, kb1, acc);
+}
+
 // Partial-sum slot of segment seg of (chunk, tile) ct: max_segs slots a
 // statically split tile, then dyn_nu a tile of the dynamic tail.
 __device__ __forceinline__ size_t part_slot(const Gemv& d, long long ct, int seg) {
@@ -234,10 +323,11 @@ __device__ void gemv_tail(const Gemv& d, Epi epi) {
 
 constexpr int kPdlCells = 4;  // cells a CTA prefetches into L2 before it waits (programmatic launch)
 
-// (register budgets: 8-token tiles 128, 16-token 170, 32-token 256 a thread,
-// so that 4, 3 and 2 CTAs an SM keep their loads in flight)
+// (register budgets: 128 a thread at 8 and 16 tokens, 170 at 32, so that 4,
+// 4 and 3 CTAs an SM keep their weight loads in flight; the 16- and 32-token
+// forms stage the activations in shared memory)
 template <int TT>
-__global__ void __launch_bounds__(kThreads, TT == 1 ? 4 : TT == 2 ? 3 : 2) splitk_kernel(Gemv d, void* C, int c_fp32, float alpha, int pdl) {
+__global__ void __launch_bounds__(kThreads, TT == 1 ? 4 : TT == 2 ? 4 : 3) splitk_kernel(Gemv d, void* C, int c_fp32, float alpha, int pdl) {
   if (pdl) {
     // Launched while the kernel that writes A still runs: the weights of this
     // CTA's first cells go into L2 (a thread a 128-byte line), then the wait.
