@@ -194,11 +194,14 @@ __device__ __forceinline__ void gemv_segment_smem(const Gemv& d, int chunk, int 
   __syncthreads();  // (the buffers are rewritten by the next segment)
 }
 
-template <int TT>
+// kStage: the activations staged in shared memory (gemv_segment_smem), else
+// held in registers (gemv_segment_regs; 8-token tiles only)
+template <int TT, bool kStage>
 __device__ __forceinline__ void gemv_segment(const Gemv& d, int chunk, int tile, int kb0, int kb1,
                                              float (&acc)[TT][4]) {
-  if constexpr (TT == 1) gemv_segment_regs<TT>(d, chunk, tile, kb0, kb1, acc);
-  else gemv_segment_smem<TT>(d, chunk, tile, kb0, kb1, acc);
+  static_assert(kStage || TT == 1, "wider tiles stage their activations");
+  if constexpr (kStage) gemv_segment_smem<TT>(d, chunk, tile, kb0, kb1, acc);
+  else gemv_segment_regs<TT>(d, chunk, tile, kb0, kb1, acc);
 }
 
 // Partial-sum slot of segment seg of (chunk, tile) ct: max_segs slots a
@@ -273,7 +276,7 @@ __device__ bool finish_segment(const Gemv& d, long long ct, int seg, int nseg, c
 // Runs this CTA's statically assigned cells.  epi(token, row, value)
 // receives every finished output; on_tile() is called (by all threads, after
 // the epilogue of a tile) in the CTA that completed a (chunk, tile).
-template <int TT, class Epi, class OnTile>
+template <int TT, bool kStage, class Epi, class OnTile>
 __device__ void gemv_streamk(const Gemv& d, Epi epi, OnTile on_tile) {
   const int c = blockIdx.x;
   long long cur = (long long)c * d.total / d.G;
@@ -286,7 +289,7 @@ __device__ void gemv_streamk(const Gemv& d, Epi epi, OnTile on_tile) {
     const int first = cta_of_cell(ct * d.nkb, d.total, d.G);
     const int nseg = cta_of_cell(ct * d.nkb + d.nkb - 1, d.total, d.G) - first + 1;
     float acc[TT][4];
-    gemv_segment<TT>(d, chunk, tile, kb0, kb1, acc);
+    gemv_segment<TT, kStage>(d, chunk, tile, kb0, kb1, acc);
     if (finish_segment<TT>(d, ct, c - first, nseg, acc, epi)) on_tile();
     cur += kb1 - kb0;
   }
@@ -295,7 +298,7 @@ __device__ void gemv_streamk(const Gemv& d, Epi epi, OnTile on_tile) {
 // The dynamic tail: units of dyn_unit k-blocks of the last dyn_tiles (chunk,
 // tile)s, taken one at a time from the unit counter; the last CTA to leave
 // resets both tail counters for the next call.
-template <int TT, class Epi>
+template <int TT, bool kStage, class Epi>
 __device__ void gemv_tail(const Gemv& d, Epi epi) {
   __shared__ int s_unit;
   const long long n_ct = (long long)d.n_chunks * d.n_tiles;
@@ -311,7 +314,7 @@ __device__ void gemv_tail(const Gemv& d, Epi epi) {
     const int seg = u % d.dyn_nu;
     const int kb0 = seg * d.dyn_unit, kb1 = min(d.nkb, kb0 + d.dyn_unit);
     float acc[TT][4];
-    gemv_segment<TT>(d, (int)(ct / d.n_tiles), (int)(ct % d.n_tiles), kb0, kb1, acc);
+    gemv_segment<TT, kStage>(d, (int)(ct / d.n_tiles), (int)(ct % d.n_tiles), kb0, kb1, acc);
     finish_segment<TT>(d, ct, seg, d.dyn_nu, acc, epi);
   }
   // every CTA's last take came before its count here: the last one resets
@@ -324,8 +327,8 @@ __device__ void gemv_tail(const Gemv& d, Epi epi) {
 constexpr int kPdlCells = 4;  // cells a CTA prefetches into L2 before it waits (programmatic launch)
 
 // (register budgets: 128 a thread at 8 and 16 tokens, 170 at 32, so that 4,
-// 4 and 3 CTAs an SM keep their weight loads in flight; the 16- and 32-token
-// forms stage the activations in shared memory)
+// 4 and 3 CTAs an SM keep their weight loads in flight, with the activations
+// staged in shared memory)
 template <int TT>
 __global__ void __launch_bounds__(kThreads, TT == 1 ? 4 : TT == 2 ? 4 : 3) splitk_kernel(Gemv d, void* C, int c_fp32, float alpha, int pdl) {
   if (pdl) {
@@ -349,8 +352,10 @@ __global__ void __launch_bounds__(kThreads, TT == 1 ? 4 : TT == 2 ? 4 : 3) split
     else
       reinterpret_cast<__nv_bfloat16*>(C)[(size_t)n * d.N + r] = __float2bfloat16_rn(v);
   };
-  gemv_streamk<TT>(d, epi, [] {});
-  if (d.dyn_tiles > 0) gemv_tail<TT>(d, epi);
+  // (staged activations at every width: measured faster for the projection,
+  // the router's 8-token form keeps them in registers)
+  gemv_streamk<TT, true>(d, epi, [] {});
+  if (d.dyn_tiles > 0) gemv_tail<TT, true>(d, epi);
 }
 
 // ------------------------------------------------------------------ router
@@ -596,7 +601,7 @@ __global__ void __launch_bounds__(kThreads, TT == 1 ? 4 : TT == 2 ? 3 : 2) route
   }
   // (2) logits
   auto epi = [&](int n, int row, float v) { r.logits[(size_t)n * r.E + row] = v; };
-  gemv_streamk<TT>(d, epi, [] {});
+  gemv_streamk<TT, (TT > 1)>(d, epi, [] {});
   // (3) the last F CTAs to finish their logits route the tokens (one warp per
   // token), once every CTA's logits are in; the last of them (or the only one,
   // from its own shared memory) builds the route order.  Every CTA of this
