@@ -110,8 +110,8 @@ __device__ __forceinline__ void gemv_segment_regs(const Gemv& d, int chunk, int 
 // Hands over the sums of segment seg (of nseg) of (chunk, tile) ct that this
 // CTA computed: written out directly when the tile has one segment, else
 // stored as partial sums; the CTA that stores a tile's last segment adds them
-// all in segment order (deterministic) and writes the tile.  Returns whether
-// this CTA completed the tile.  Called by all threads.
+// all in segment order (deterministic) and writes the tile.  Called by all
+// threads.
 constexpr int kXPitch = 256 + 16;  // bytes a token row of a staged k-block (padded: no bank conflicts)
 
 MOE_DEV void cp_async16(void* dst, const void* src) {
@@ -212,7 +212,7 @@ __device__ __forceinline__ size_t part_slot(const Gemv& d, long long ct, int seg
 }
 
 template <int TT, class Epi>
-__device__ bool finish_segment(const Gemv& d, long long ct, int seg, int nseg, const float (&acc)[TT][4], Epi epi) {
+__device__ void finish_segment(const Gemv& d, long long ct, int seg, int nseg, const float (&acc)[TT][4], Epi epi) {
   __shared__ int s_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
   constexpr int kTileOut = 8 * TT * 64;
@@ -229,7 +229,7 @@ __device__ bool finish_segment(const Gemv& d, long long ct, int seg, int nseg, c
       }
     }
     __syncthreads();
-    return true;
+    return;
   }
   float* P = d.partials + part_slot(d, ct, seg) * kTileOut;
 #pragma unroll
@@ -248,7 +248,7 @@ __device__ bool finish_segment(const Gemv& d, long long ct, int seg, int nseg, c
     s_last = (old == (unsigned)(nseg - 1));
   }
   __syncthreads();
-  if (!s_last) return false;
+  if (!s_last) return;
   const float* P0 = d.partials + part_slot(d, ct, 0) * kTileOut;
   // only the valid tokens of the chunk; the segment loads of one output are
   // independent and issued 16 at a time, then added in segment order
@@ -270,14 +270,12 @@ __device__ bool finish_segment(const Gemv& d, long long ct, int seg, int nseg, c
   }
   __syncthreads();
   if (threadIdx.x == 0) d.tickets[ct] = 0u;
-  return true;
 }
 
 // Runs this CTA's statically assigned cells.  epi(token, row, value)
-// receives every finished output; on_tile() is called (by all threads, after
-// the epilogue of a tile) in the CTA that completed a (chunk, tile).
-template <int TT, bool kStage, class Epi, class OnTile>
-__device__ void gemv_streamk(const Gemv& d, Epi epi, OnTile on_tile) {
+// receives every finished output.
+template <int TT, bool kStage, class Epi>
+__device__ void gemv_streamk(const Gemv& d, Epi epi) {
   const int c = blockIdx.x;
   long long cur = (long long)c * d.total / d.G;
   const long long end = (long long)(c + 1) * d.total / d.G;
@@ -290,7 +288,7 @@ __device__ void gemv_streamk(const Gemv& d, Epi epi, OnTile on_tile) {
     const int nseg = cta_of_cell(ct * d.nkb + d.nkb - 1, d.total, d.G) - first + 1;
     float acc[TT][4];
     gemv_segment<TT, kStage>(d, chunk, tile, kb0, kb1, acc);
-    if (finish_segment<TT>(d, ct, c - first, nseg, acc, epi)) on_tile();
+    finish_segment<TT>(d, ct, c - first, nseg, acc, epi);
     cur += kb1 - kb0;
   }
 }
@@ -354,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, TT == 1 ? 4 : TT == 2 ? 4 : 3) split
   };
   // (staged activations at every width: measured faster for the projection,
   // the router's 8-token form keeps them in registers)
-  gemv_streamk<TT, true>(d, epi, [] {});
+  gemv_streamk<TT, true>(d, epi);
   if (d.dyn_tiles > 0) gemv_tail<TT, true>(d, epi);
 }
 
@@ -601,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, TT == 1 ? 4 : TT == 2 ? 3 : 2) route
   }
   // (2) logits
   auto epi = [&](int n, int row, float v) { r.logits[(size_t)n * r.E + row] = v; };
-  gemv_streamk<TT, (TT > 1)>(d, epi, [] {});
+  gemv_streamk<TT, (TT > 1)>(d, epi);
   // (3) the last F CTAs to finish their logits route the tokens (one warp per
   // token), once every CTA's logits are in; the last of them (or the only one,
   // from its own shared memory) builds the route order.  Every CTA of this
