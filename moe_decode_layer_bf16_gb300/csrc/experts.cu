@@ -239,8 +239,6 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
     uint32_t ph = 0;         // parity of slot si's current use
     bool alive = true;
     int item = 0;
-    int pre_slot = -1, pre_val = 0;  // lane 0: readiness of the next item's expert, loaded ahead
-    int pre_done = 0;                // lane 0: w13 items finished, loaded ahead
     bool all_ready = false;          // every w13 item (and every h group) is done
     // until the routing is loaded only the shared expert's w13 items are known
     bool routed = false;
@@ -312,8 +310,13 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
       // counted epilogues published; a generic-to-async proxy fence then
       // orders the TMA reads of h after them)
       if (!it.a && !all_ready) {
-        // all w13 work done (lane 0's acquire of the count): covers every expert from now on
-        if (__shfl_sync(0xffffffffu, lane == 0 && pre_done >= totA ? 1 : 0, 0)) {
+        // all w13 work done (lane 0's acquire of the count): covers every expert
+        // from now on.  (Loading this count and the next expert's a stage ahead,
+        // mid-item, measured 1.3% slower at 8 tokens: the acquires stall the
+        // copies of the item in flight.)
+        int done = 0;
+        if (lane == 0) done = ld_acquire(p.hdr + kHdrDoneA);
+        if (__shfl_sync(0xffffffffu, lane == 0 && done >= totA ? 1 : 0, 0)) {
           all_ready = true;
           asm volatile("fence.proxy.async.global;" ::: "memory");
         }
@@ -322,18 +325,16 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
         // w2 items need the expert's quantised h: all of its groups
         int sk = 0;
         if (lane == 0) {
-          if (!(pre_slot == it.slot && pre_val >= nkbK)) {
-            const unsigned long long t0 = globaltimer_ns();
-            for (long n = 0;; ++n) {
-              if (ld_acquire(p.ready + it.slot) >= nkbK) break;
-              if (*(volatile int*)status != 0 || n > (1l << 24)) { sk = 1; break; }
-              if (globaltimer_ns() - t0 > kWaitNs) {
-                atomicExch(status, MOE_ERR_DEVICE_TIMEOUT);
-                sk = 1;
-                break;
-              }
-              __nanosleep(64);
+          const unsigned long long t0 = globaltimer_ns();
+          for (long n = 0;; ++n) {
+            if (ld_acquire(p.ready + it.slot) >= nkbK) break;
+            if (*(volatile int*)status != 0 || n > (1l << 24)) { sk = 1; break; }
+            if (globaltimer_ns() - t0 > kWaitNs) {
+              atomicExch(status, MOE_ERR_DEVICE_TIMEOUT);
+              sk = 1;
+              break;
             }
+            __nanosleep(64);
           }
           if (!sk) s_rdy[it.slot] = 1;
         }
@@ -368,7 +369,6 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
         if (!xt && lane < ntok)
           xsrc = it.a ? p.xq + (size_t)token_of(p, tb, s, pass * kTok + lane) * p.H
                       : p.hq + (size_t)(s.hbase + pass * kTok + lane) * p.Imax;
-        const int la_st = min(2, nstage - 1);  // stage that looks ahead at the next item
         int qr = it.a ? 0 : it.q0, kb0 = 0;    // row quarter and first k-block of stage st
         for (int st = 0; st < (skip ? 1 : nstage); ++st) {
           int ok = 1;
@@ -420,18 +420,6 @@ __global__ void __launch_bounds__(Cfg<TT>::kThreads, 1) experts_kernel(ExpertArg
                 uint8_t* xd = xdst + h * C::kXHalf;
                 if (it.a) tma_load_3d(xd, &maps.xq, 0, kh, pass * kTok, full + si);
                 else tma_load_3d(xd, &maps.hq, 0, kh, s.hbase + pass * kTok, full + si);
-              }
-            }
-          }
-          if (lane == 0 && pass == 0 && st == la_st && nxt < total) {
-            // look ahead: load the readiness of the next item's expert now, so
-            // that a w2 item rarely waits on a round trip when it starts
-            const Item nit = decode_item(nxt, nA_sh, nA_r, totA, nB, has_shared, p.bq);
-            if (!nit.a && !all_ready) {
-              pre_done = ld_acquire(p.hdr + kHdrDoneA);
-              if (!s_rdy[nit.slot]) {
-                pre_slot = nit.slot;
-                pre_val = ld_acquire(p.ready + nit.slot);
               }
             }
           }
