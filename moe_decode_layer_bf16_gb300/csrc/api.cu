@@ -328,8 +328,11 @@ static int layer_impl(const moe_layer_dims* dims, const moe_layer_weights* w, in
   ea.router_ctas = plan.G;
   // a w2 item streams its 32-row groups over all of I: 4 of them (a whole
   // scale block) unless the rows are long (I >= 8192, a dense layer's MLP),
-  // where single groups keep the queue's tail short
-  ea.bq = L.Imax >= 8192 ? 1 : 4;
+  // where single groups keep the queue's tail short, or the whole-block items
+  // would give the SMs no more than 4 each (one token's 8 experts and the
+  // shared one: 504 items over 152 SMs), where half blocks even out the tail
+  const long long w2_items = (std::min<long long>((long long)M * k, E) + (dims->shared_inter > 0 ? 1 : 0)) * (H / kBlock);
+  ea.bq = L.Imax >= 8192 ? 1 : (w2_items <= 4LL * sms ? 2 : 4);
   // every expert-kernel launch parameter is prepared before the router is
   // enqueued, so that no host work delays the expert kernel behind it
   const bool tc = expert_path(*dims, M) == MOE_PATH_TCGEN05;

@@ -142,7 +142,7 @@ MOE_DEV Item decode_item(int item, int nA_sh, int nA_r, int totA, int nB, bool h
     else { const int j = item - nA_sh; it.slot = j / nA_r + (has_shared ? 1 : 0); it.idx = j % nA_r; }
   } else {
     it.a = false;
-    const int lp = bq == 4 ? 0 : 2;  // log2 of the items per 128-row block
+    const int lp = bq == 4 ? 0 : bq == 2 ? 1 : 2;  // log2 of the items per 128-row block
     const int j = item - totA;
     it.slot = j / (nB << lp);
     const int r = j - it.slot * (nB << lp);

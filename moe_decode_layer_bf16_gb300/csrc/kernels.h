@@ -130,7 +130,7 @@ struct ExpertArgs {
   float* h; uint8_t* hq; float* hs;
   float* rows; float* shared_out;
   int router_ctas;  // CTAs of the router launch that precedes this kernel
-  int bq;           // w2 item size in 32-row quarters of a 128-row block: 4, or 1 for long rows
+  int bq;           // w2 item size in 32-row quarters of a 128-row block: 4, 2 or 1
 };
 // An expert-kernel launch prepared on the host (tensor maps encoded, the
 // pass width and ring depth chosen, the shared-memory limit set) before the
