@@ -63,15 +63,16 @@ EXPERT_BYTES = 2 * DSV3.inter * DSV3.hidden + DSV3.hidden * DSV3.inter + 4 * (
 ROUTER_BYTES = DSV3.num_experts * DSV3.hidden * 2
 # DRAM bytes (read + write) per activated expert of one launch of each expert
 # kernel, from the ncu capture of profiles/experts_kernels_dsv3_e32_traffic.txt
-# (the 32-expert profiling layer: experts_kernel at 8 tokens, 29 experts active,
-# experts_tc_kernel at 32 tokens, 33 experts active), valid for the source whose
+# (the 32-expert profiling layer: experts_kernel at 1 and 8 tokens, 9 and 29
+# experts active, the mean of the two per-expert figures; experts_tc_kernel at
+# 32 tokens, 33 experts active), valid for the source whose
 # code (comments and white space removed) has the SHA-256 given; the bench
 # reports no traffic once a kernel's code differs from the captured one.
 TRAFFIC_CAPTURE = {
-    "experts.cu": {"code_sha256": "14d5e9187e63fb866cf77d6c09788abf1a603ee01e0c7a5c8fae1265a3b75c12",
-                   "bytes_per_expert": 44_167_471},
+    "experts.cu": {"code_sha256": "17d19129ee3d3d1e85b402138301d65921218ba69a2e5ad5d5b5c311cb89abff",
+                   "bytes_per_expert": 44_148_562},
     "experts_tc.cu": {"code_sha256": "0513010fb4821d17177604fa276254241b5d02755c2e3798dc9f5a0fecd111fa",
-                      "bytes_per_expert": 44_370_227},
+                      "bytes_per_expert": 44_370_148},
 }
 
 
