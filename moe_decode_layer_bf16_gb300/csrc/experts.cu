@@ -20,7 +20,8 @@
 //     shared expert first, then all w2 items):
 //       A item (expert, 16 intermediates): 16 gate + 16 up rows of w13 over H,
 //       B item (expert, 128 rows of w2, one scale block) over I, streamed as
-//       four 32-row groups (one group per item when I is long: a dense MLP);
+//       four 32-row groups (two per item when the whole-block items would be
+//       too few to spread over the SMs, one when I is long: a dense MLP);
 //   * a stage is 8 k-blocks (1024 columns): two 16 KB TMA boxes of weights
 //     (128-byte swizzle) plus the pass's FP8 activation columns (TMA boxes of
 //     the shared expert's x rows, or one 1-D bulk copy per token row), all
