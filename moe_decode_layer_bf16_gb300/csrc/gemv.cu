@@ -556,42 +556,63 @@ __global__ void __launch_bounds__(kThreads, TT == 1 ? 4 : TT == 2 ? 3 : 2) route
         r.hdr[kHdrDoneA] = 0;
       }
     }
-    // one warp per 1024-column slice of a token (8 groups): lane l holds
-    // columns [32 l, 32 l + 32) of the slice, a group is 4 lanes
     const int nkbH = r.H / kBlock;
     const int nsl = (nkbH + 7) / 8;  // slices per token
     const uint16_t* x = reinterpret_cast<const uint16_t*>(d.A);
-    for (int si = blockIdx.x * (kThreads / 32) + warp; si < d.M * nsl; si += gridDim.x * (kThreads / 32)) {
-      const int t = si / nsl, c0 = (si % nsl) * 1024 + 32 * lane;
-      const bool on = c0 < r.H;
-      uint4 raw[4];
+    if (d.M * nkbH <= (int)gridDim.x * (kThreads / 32)) {
+      // a few tokens: one warp per 128-column group (lane l holds columns
+      // [4 l, 4 l + 4)), taken from the grid's last CTA down, so that the
+      // CTAs that quantise, and start their logits after it, lose little
+      // (one warp per 1024 columns kept two CTAs about 3 us behind the
+      // others at one token, and the routing waits for the last logits)
+      const int gi = ((int)gridDim.x - 1 - (int)blockIdx.x) * (kThreads / 32) + warp;
+      if (gi < d.M * nkbH) {
+        const int t = gi / nkbH, c0 = (gi % nkbH) * kBlock + 4 * lane;
+        const uint2 raw = __ldg(reinterpret_cast<const uint2*>(x + (size_t)t * r.H + c0));
+        const float v0 = bf16_lo(raw.x), v1 = bf16_hi(raw.x), v2 = bf16_lo(raw.y), v3 = bf16_hi(raw.y);
+        float amax = fmaxf(fmaxf(fabsf(v0), fabsf(v1)), fmaxf(fabsf(v2), fabsf(v3)));
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
-        raw[j] = on ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * r.H + c0 + 8 * j)) : make_uint4(0, 0, 0, 0);
-      float v[32];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        v[8 * j + 0] = bf16_lo(raw[j].x); v[8 * j + 1] = bf16_hi(raw[j].x);
-        v[8 * j + 2] = bf16_lo(raw[j].y); v[8 * j + 3] = bf16_hi(raw[j].y);
-        v[8 * j + 4] = bf16_lo(raw[j].z); v[8 * j + 5] = bf16_hi(raw[j].z);
-        v[8 * j + 6] = bf16_lo(raw[j].w); v[8 * j + 7] = bf16_hi(raw[j].w);
-      }
-      float amax = 0.f;
-#pragma unroll
-      for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-      amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-      if (on) {
+        for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         const float sc = group_scale(amax, r.e8m0);
-        uint32_t q[8];
+        *reinterpret_cast<uint32_t*>(r.xq + (size_t)t * r.H + c0) =
+            f32x4_to_e4m3x4(__fdiv_rn(v0, sc), __fdiv_rn(v1, sc), __fdiv_rn(v2, sc), __fdiv_rn(v3, sc));
+        if (lane == 0) r.xs[(size_t)t * nkbH + gi % nkbH] = sc;
+      }
+    } else {
+      // one warp per 1024-column slice of a token (8 groups): lane l holds
+      // columns [32 l, 32 l + 32) of the slice, a group is 4 lanes
+      for (int si = blockIdx.x * (kThreads / 32) + warp; si < d.M * nsl; si += gridDim.x * (kThreads / 32)) {
+        const int t = si / nsl, c0 = (si % nsl) * 1024 + 32 * lane;
+        const bool on = c0 < r.H;
+        uint4 raw[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          q[j] = f32x4_to_e4m3x4(__fdiv_rn(v[4 * j], sc), __fdiv_rn(v[4 * j + 1], sc), __fdiv_rn(v[4 * j + 2], sc),
-                                 __fdiv_rn(v[4 * j + 3], sc));
-        uint8_t* dst = r.xq + (size_t)t * r.H + c0;
-        *reinterpret_cast<uint4*>(dst) = make_uint4(q[0], q[1], q[2], q[3]);
-        *reinterpret_cast<uint4*>(dst + 16) = make_uint4(q[4], q[5], q[6], q[7]);
-        if ((lane & 3) == 0) r.xs[(size_t)t * nkbH + c0 / kBlock] = sc;
+        for (int j = 0; j < 4; ++j)
+          raw[j] = on ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * r.H + c0 + 8 * j)) : make_uint4(0, 0, 0, 0);
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[8 * j + 0] = bf16_lo(raw[j].x); v[8 * j + 1] = bf16_hi(raw[j].x);
+          v[8 * j + 2] = bf16_lo(raw[j].y); v[8 * j + 3] = bf16_hi(raw[j].y);
+          v[8 * j + 4] = bf16_lo(raw[j].z); v[8 * j + 5] = bf16_hi(raw[j].z);
+          v[8 * j + 6] = bf16_lo(raw[j].w); v[8 * j + 7] = bf16_hi(raw[j].w);
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(v[j]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        if (on) {
+          const float sc = group_scale(amax, r.e8m0);
+          uint32_t q[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            q[j] = f32x4_to_e4m3x4(__fdiv_rn(v[4 * j], sc), __fdiv_rn(v[4 * j + 1], sc), __fdiv_rn(v[4 * j + 2], sc),
+                                   __fdiv_rn(v[4 * j + 3], sc));
+          uint8_t* dst = r.xq + (size_t)t * r.H + c0;
+          *reinterpret_cast<uint4*>(dst) = make_uint4(q[0], q[1], q[2], q[3]);
+          *reinterpret_cast<uint4*>(dst + 16) = make_uint4(q[4], q[5], q[6], q[7]);
+          if ((lane & 3) == 0) r.xs[(size_t)t * nkbH + c0 / kBlock] = sc;
+        }
       }
     }
     __syncthreads();
